@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of the KV-cache compression hot path on GB300.
+
+One step = one pass of every hot-path row over one batch of synthetic input,
+all inputs resident in HBM when the timed region starts:
+  KIVI INT4 workload (batch 8, 8 KV heads, T 8192, head_dim 128, bf16):
+    quantize K (per channel, groups of 64 tokens) and V (per token, groups of
+    64 channels), asymmetric [0, 15], bf16 scale + zero, 128-token bf16
+    residual window; dequantize both; error statistics of both;
+  eviction workload (32 heads, history fp32 [64 steps, T 131072], B 2048,
+    W 128): H2O select + compaction of K and V, SnapKV select (mean of the
+    last 32 steps) + compaction of K and V.
+The L2 is flushed (a 2x-L2 buffer is written) before every phase, outside the
+CUDA-event intervals that time the phases.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV quant+dequant GB/s & % of GB300 HBM peak; H2O select+compact tokens/s"
+UNIT = "GB/s"
+SPEC_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# workload constants
+KIVI = dict(batch=8, heads=8, T=8192, D=128, g=64, R=128)
+EVICT = dict(heads=32, steps=64, T=131072, D=128, budget=2048, window=128, obs=32)
+WORKLOAD_NAME = ("kivi_int4[b8,h8,T8192,d128,g64,R128] + h2o/snapkv[h32,S64,T131072,d128,B2048,W128,obs32]")
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+
+def kivi_bytes():
+    """Per step, K and V together (read + write bytes the method must move)."""
+    outer, T, D, g, R = KIVI["batch"] * KIVI["heads"], KIVI["T"], KIVI["D"], KIVI["g"], KIVI["R"]
+    Tq = T - R
+    x = outer * T * D * 2
+    codes = outer * Tq * D // 2
+    meta = (outer * (Tq // g) * D) * 2 * 2          # K: bf16 scale + zero per (group, channel)
+    meta_v = (outer * Tq * (D // g)) * 2 * 2        # V: per (token, group)
+    resid = outer * R * D * 2
+    quant = 2 * x // 2 + (codes + meta + resid) + (codes + meta_v + resid)   # read x(K,V) + writes
+    quant = x * 2 + codes * 2 + meta + meta_v + resid * 2
+    dequant = quant                                                           # reverse direction
+    stats = x * 2 + codes * 2 + meta + meta_v                                 # residual error is zero: not read
+    return dict(quantize=quant, dequantize=dequant, error_stats=stats)
+
+
+def evict_bytes():
+    H, S, T, D, B, obs = (EVICT[k] for k in ("heads", "steps", "T", "D", "budget", "obs"))
+    keep = H * B * 4
+    compact = 2 * (2 * H * B * D * 2)                 # K and V: read kept rows + write them
+    return dict(h2o_select=H * S * T * 4 + keep, h2o_compact=compact,
+                snapkv_select=H * obs * T * 4 + keep, snapkv_compact=compact)
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kv_cache_quantization_kvq_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the dominant call, from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("source_digest") == source_digest():
+            return d.get("traffic_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the GPU step
+
+class Step:
+    """Device buffers and the launches of one step, through the C ABI."""
+
+    def __init__(self, b, dev, stream):
+        import torch
+        from kv_cache_quantization_kvq_gb300 import workloads as W
+        self.b, self.dev, self.stream = b, dev, stream
+        outer = KIVI["batch"] * KIVI["heads"]
+        self.kshape = (outer, KIVI["T"], KIVI["D"])
+        self.K, self.V = W.kivi_kv(dev, seed=2, batch=KIVI["batch"], heads=KIVI["heads"], T=KIVI["T"], D=KIVI["D"])
+        self.qpK = b.QParams.asym(4, 0, 15, axis=b.ALONG_T, group=KIVI["g"], residual=KIVI["R"],
+                                  scale_dtype=b.BF16, zero_dtype=b.BF16)
+        self.qpV = b.QParams.asym(4, 0, 15, axis=b.ALONG_C, group=KIVI["g"], residual=KIVI["R"],
+                                  scale_dtype=b.BF16, zero_dtype=b.BF16)
+        self.qK, self.wsK = b.alloc_quantized(self.kshape, b.BF16, self.qpK, dev)
+        self.qV, self.wsV = b.alloc_quantized(self.kshape, b.BF16, self.qpV, dev)
+        self.dK = torch.empty_like(self.K)
+        self.dV = torch.empty_like(self.V)
+        self.stK = torch.zeros(3, dtype=torch.float64, device=dev)
+        self.stV = torch.zeros(3, dtype=torch.float64, device=dev)
+        H, S, T, D = EVICT["heads"], EVICT["steps"], EVICT["T"], EVICT["D"]
+        self.hist, self.EK, self.EV = W.eviction_inputs(dev, seed=5, heads=H, steps=S, T=T, D=D,
+                                                        window=EVICT["window"])
+        self.keep = torch.empty((H, EVICT["budget"]), dtype=torch.int32, device=dev)
+        self.skeep = torch.empty_like(self.keep)
+        self.selB = b.kv_select_workspace(H, T)
+        self.sel_ws = torch.empty(self.selB, dtype=torch.uint8, device=dev)
+        self.cK = torch.empty((H, EVICT["budget"], D), dtype=torch.bfloat16, device=dev)
+        self.cV = torch.empty_like(self.cK)
+        self.scK = torch.empty_like(self.cK)
+        self.scV = torch.empty_like(self.cK)
+        torch.cuda.synchronize()
+
+    # each phase returns the number of kernels it launched
+    def quantize(self):
+        b, s = self.b, self.stream
+        b.kvq_quantize(self.K, b.BF16, self.kshape, self.qpK, self.qK.codes, self.qK.scale, self.qK.zero,
+                       self.qK.resid, self.wsK, self.wsK.numel(), s)
+        b.kvq_quantize(self.V, b.BF16, self.kshape, self.qpV, self.qV.codes, self.qV.scale, self.qV.zero,
+                       self.qV.resid, self.wsV, self.wsV.numel(), s)
+        return 2
+
+    def dequantize(self):
+        b, s = self.b, self.stream
+        b.kvq_dequantize(self.qK.codes, self.qK.scale, self.qK.zero, self.qK.resid, self.kshape, self.qpK,
+                         self.dK, b.BF16, s)
+        b.kvq_dequantize(self.qV.codes, self.qV.scale, self.qV.zero, self.qV.resid, self.kshape, self.qpV,
+                         self.dV, b.BF16, s)
+        return 2
+
+    def error_stats(self):
+        b, s = self.b, self.stream
+        b.kvq_error_stats(self.K, b.BF16, self.qK.codes, self.qK.scale, self.qK.zero, self.qK.resid,
+                          self.kshape, self.qpK, self.stK, self.wsK, self.wsK.numel(), s)
+        b.kvq_error_stats(self.V, b.BF16, self.qV.codes, self.qV.scale, self.qV.zero, self.qV.resid,
+                          self.kshape, self.qpV, self.stV, self.wsV, self.wsV.numel(), s)
+        return 4          # two stats kernels + two finalize kernels
+
+    def h2o_select(self):
+        b, H, S, T = self.b, EVICT["heads"], EVICT["steps"], EVICT["T"]
+        b.kv_h2o_select(self.hist, H, S, T, EVICT["budget"], EVICT["window"], self.keep, None, self.sel_ws,
+                        self.selB, self.stream)
+        return 8
+
+    def h2o_compact(self):
+        b, H, T, D = self.b, EVICT["heads"], EVICT["T"], EVICT["D"]
+        b.kv_compact(self.EK, b.BF16, H, T, D, self.keep, EVICT["budget"], self.cK, self.stream)
+        b.kv_compact(self.EV, b.BF16, H, T, D, self.keep, EVICT["budget"], self.cV, self.stream)
+        return 2
+
+    def snapkv_select(self):
+        b, H, S, T = self.b, EVICT["heads"], EVICT["steps"], EVICT["T"]
+        b.kv_snapkv_select(self.hist, H, S, T, EVICT["obs"], EVICT["budget"], EVICT["window"], self.skeep, None,
+                           self.sel_ws, self.selB, self.stream)
+        return 8
+
+    def snapkv_compact(self):
+        b, H, T, D = self.b, EVICT["heads"], EVICT["T"], EVICT["D"]
+        b.kv_compact(self.EK, b.BF16, H, T, D, self.skeep, EVICT["budget"], self.scK, self.stream)
+        b.kv_compact(self.EV, b.BF16, H, T, D, self.skeep, EVICT["budget"], self.scV, self.stream)
+        return 2
+
+    PHASES = ("quantize", "dequantize", "error_stats", "h2o_select", "h2o_compact", "snapkv_select",
+              "snapkv_compact")
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from kv_cache_quantization_kvq_gb300 import build as build_lib
+    build_lib()
+    from kv_cache_quantization_kvq_gb300 import binding as b
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        st = Step(b, dev, stream)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    kb, eb = kivi_bytes(), evict_bytes()
+    pbytes = {**kb, **eb}
+    phases = list(Step.PHASES)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for ph in phases:
+                flush.zero_()
+                getattr(st, ph)()
+    barrier()
+
+    K = args.steps
+    ev = {ph: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+          for ph in phases}
+    launches = 0
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                for ph in phases:
+                    flush.zero_()
+                    a, z = ev[ph][i]
+                    a.record(stream)
+                    launches += getattr(st, ph)()
+                    z.record(stream)
+        barrier()
+        wall = time.perf_counter() - t0
+    ph_ms = {ph: statistics.fmean(a.elapsed_time(z) for a, z in ev[ph]) for ph in phases}
+    step_ms = sum(ph_ms.values())
+    if world > 1:
+        t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    total_bytes = sum(pbytes.values())
+    value = world * total_bytes / (step_ms * 1e-3) / 1e9
+
+    # sanity of the step's outputs (not timed): selection sizes, finite stats
+    torch.cuda.synchronize()
+    assert torch.isfinite(st.stK).all() and torch.isfinite(st.stV).all()
+
+    result = None
+    if rank == 0:
+        peak, peak_kind = measured_peak()
+        h2o_ms = ph_ms["h2o_select"] + ph_ms["h2o_compact"]
+        tokens = EVICT["heads"] * EVICT["T"]
+        sel_B = pbytes["h2o_select"]
+        sel_gbs = sel_B / (ph_ms["h2o_select"] * 1e-3) / 1e9
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16/f32 in, int4 codes; f32 arithmetic",
+            "data": "synthetic (seeded generators; shapes and distributions of the pages' workloads)",
+            "config": {"workload": WORKLOAD_NAME, "l2": "flushed (2x L2 written) before every phase, outside the timed intervals",
+                       "inputs_resident_in_hbm": True, "parallelism": f"weak: {world} independent replica(s)"},
+            "hbm_frac_of_8TBs": round(value / world / SPEC_HBM_GBS, 4),
+            "hbm_frac_of_measured": round(value / world / peak, 4),
+            "h2o_tokens_per_s": round(world * tokens / (h2o_ms * 1e-3), 1),
+            "phases": {ph: {"ms": round(ph_ms[ph], 5), "GB/s": round(pbytes[ph] / (ph_ms[ph] * 1e-3) / 1e9, 1),
+                            "bytes": pbytes[ph]} for ph in phases},
+            "roofline": {"kernel": "kv_h2o_select (colsum_hist_kernel + L2-resident radix select)",
+                         "bound": "hbm", "achieved": round(sel_gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(sel_gbs / peak, 4), "peak_kind": f"of {peak_kind}",
+                         "bytes_per_launch": sel_B, "traffic": ncu_traffic()},
+            "gpu_launches": launches,
+            "wall_s_timed_region": round(wall, 3),
+            "clocks": clk.summary(),
+        }
+        if not args.no_e2e:
+            result["e2e"] = run_e2e(b, st, stream, dev, args, total_bytes, world)
+        if not args.no_cpu_baseline and world == 1:
+            result["cpu_baseline"] = cpu_baseline(min_seconds=args.cpu_seconds)
+    return result
+
+
+def run_e2e(b, st, stream, dev, args, total_bytes, world):
+    """Same step through the C ABI with host buffers: pinned host -> device
+    copies of every input, the step, device -> host copies of the results."""
+    import torch
+    ins = [st.K, st.V, st.hist, st.EK, st.EV]
+    host_in = [t.cpu().pin_memory() for t in ins]
+    outs = [st.qK.codes, st.qK.scale, st.qK.zero, st.qK.resid, st.qV.codes, st.qV.scale, st.qV.zero,
+            st.qV.resid, st.stK, st.stV, st.keep, st.skeep, st.cK, st.cV, st.scK, st.scV]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    n = max(3, min(args.steps, args.e2e_steps))
+
+    def one():
+        for d, h in zip(ins, host_in):
+            d.copy_(h, non_blocking=True)
+        for ph in Step.PHASES:
+            getattr(st, ph)()
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            one()
+        z.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(z) / n
+    return {"value": round(world * total_bytes / (ms * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+# ---------------------------------------------------------------- the oracle (CPU)
+
+def oracle_sample(seed=0):
+    """One [outer] slice of the KIVI workload and one head of the eviction
+    workload, drawn on the host with the same recipes."""
+    from kv_cache_quantization_kvq_gb300 import workloads as W
+    rng = np.random.default_rng(seed)
+    T, D = KIVI["T"], KIVI["D"]
+    xk = W.to_bf16_bits(W.random_kv(rng, (1, T, D), 0.02, 8.0))
+    xv = W.to_bf16_bits(rng.standard_normal((1, T, D), dtype=np.float32))
+    ET = EVICT["T"]
+    hist = W.random_history(rng, 1, EVICT["steps"], ET, planted=256, window=EVICT["window"])
+    ek = W.to_bf16_bits(rng.standard_normal((1, ET, D), dtype=np.float32))
+    ev = W.to_bf16_bits(rng.standard_normal((1, ET, D), dtype=np.float32))
+    return xk, xv, hist, ek, ev
+
+
+def oracle_step(sample):
+    import oracle as O
+    xk, xv, hist, ek, ev = sample
+    qk = O.QParams.asym(4, 0, 15, axis=O.ALONG_T, group=KIVI["g"], residual=KIVI["R"], scale_dtype=O.BF16,
+                        zero_dtype=O.BF16)
+    qv = O.QParams.asym(4, 0, 15, axis=O.ALONG_C, group=KIVI["g"], residual=KIVI["R"], scale_dtype=O.BF16,
+                        zero_dtype=O.BF16)
+    a, c = O.quantize(xk, O.BF16, qk), O.quantize(xv, O.BF16, qv)
+    O.dequantize(a, xk.shape, qk, O.BF16)
+    O.dequantize(c, xv.shape, qv, O.BF16)
+    O.error_stats(xk, O.BF16, a, qk)
+    O.error_stats(xv, O.BF16, c, qv)
+    keep, _ = O.h2o_select(hist, EVICT["budget"], EVICT["window"])
+    O.compact(ek, keep)
+    O.compact(ev, keep)
+    skeep, _ = O.snapkv_select(hist, EVICT["obs"], EVICT["budget"], EVICT["window"])
+    O.compact(ek, skeep)
+    O.compact(ev, skeep)
+    outer = KIVI["batch"] * KIVI["heads"]
+    kb, eb = kivi_bytes(), evict_bytes()
+    return sum(kb.values()) / outer + sum(eb.values()) / EVICT["heads"]
+
+
+SAMPLE_DESC = ("oracle (plain C, 1 thread) on 1 of 64 [batch*head] slices of the KIVI workload "
+               "(quantize/dequantize/error stats of K and V) plus 1 of 32 heads of the eviction "
+               "workload (H2O + SnapKV select, compaction of K and V); GB/s = the slice's algorithmic bytes / time")
+
+
+def cpu_baseline(min_seconds=10.0):
+    import oracle as O
+    O.build()
+    sample = oracle_sample(1)
+    oracle_step(sample)                     # warm
+    done, nbytes, t0 = 0, 0.0, time.perf_counter()
+    while True:
+        nbytes += oracle_step(sample)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    return {"value": round(nbytes / el / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{SAMPLE_DESC}; {done} repetitions in {el:.1f} s"}
+
+
+def run_reference(args):
+    import oracle as O
+    O.build()
+    sample = oracle_sample(1)
+    for _ in range(args.warmup):
+        oracle_step(sample)
+    times, nbytes = [], 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        nbytes += oracle_step(sample)
+        times.append(time.perf_counter() - t0)
+    el = sum(times)
+    value = nbytes / el / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 arithmetic (CPU oracle)",
+        "data": "synthetic (seeded generators, host)",
+        "config": {"workload": WORKLOAD_NAME, "sample": "one KIVI slice + one eviction head per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": SAMPLE_DESC},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

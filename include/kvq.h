@@ -1,0 +1,202 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) KV-cache compression hot path.
+ *
+ * Everything the path computes runs in hand-written CUDA kernels launched on
+ * the caller's stream.  The header needs no CUDA include: a stream is passed
+ * as `void*` (a cudaStream_t; NULL is the legacy default stream).
+ *
+ * Sources, cited by page title and section:
+ *  [FtC] "KV Compression 公式到源码对照" (formula-to-source walkthrough):
+ *        §1.1 symmetric per-channel quantization, §1.2 asymmetric
+ *        per-channel quantization, §1.3 dequantization and error metrics,
+ *        §2 compression ratio counting scale/zero-point bytes, §3.1 H2O
+ *        cumulative attention score, §3.2 recent window union heavy hitters,
+ *        §3.3 SnapKV one-shot selection, §4 token compression ratio.
+ *  [KVC] "KV cache 压缩：把历史装得更小":
+ *        §"量化：位置都留着，每个数更短" (group-wise x ~ s*(q - z); K grouped
+ *        per channel, V per token), §"4 bit 的实际压缩率由分组大小决定"
+ *        (payload plus per-group bf16 scale and zero),
+ *        §"带残差区的压缩预算，逐项加起来" (the most recent tokens stay in
+ *        bf16), §"少存 token：合并，或淘汰" (eviction frees the dropped K/V).
+ *
+ * Conventions shared by every entry point
+ *  - Ownership: every buffer pointer is a DEVICE pointer owned by the caller,
+ *    except the small descriptor structs (kvq_shape, kvq_qparams), which are
+ *    read on the host during the call and may be freed when it returns.  The
+ *    library never allocates, frees or synchronises; sizes of every output
+ *    and workspace come from kvq_quantized_sizes / kv_select_workspace.
+ *  - Asynchrony: device work is enqueued on `stream`; outputs are valid once
+ *    the stream reaches that point.  Workspace contents are scratch and must
+ *    not be shared by calls that may overlap on the GPU.
+ *  - Errors: arguments are checked on the host before anything is launched.
+ *    A rejected call returns KVQ_EINVAL (or KVQ_EWORKSPACE / KVQ_EUNSUPPORTED)
+ *    and has no side effect.  KVQ_ECUDA reports a launch failure.  The text
+ *    of the last failure on the calling thread is kvq_last_error().
+ *  - Tensors are row-major with the last axis contiguous.  A KV tensor is
+ *    viewed as [outer, T, C]: outer = batch*heads (or layers), T tokens,
+ *    C channels (head_dim, or heads*head_dim).
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_EINVAL = 1,        /* invalid argument (the pages' ValueError cases) */
+    KVQ_ECUDA = 2,         /* a CUDA launch or runtime call failed           */
+    KVQ_EUNSUPPORTED = 3,  /* valid, but not implemented                     */
+    KVQ_EWORKSPACE = 4     /* workspace missing or smaller than required     */
+} kvq_status;
+
+typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1, KVQ_I8 = 2, KVQ_NONE = 3 } kvq_dtype;
+typedef enum { KVQ_SYM = 0, KVQ_ASYM = 1 } kvq_mode;
+typedef enum {
+    KVQ_GROUP_ALONG_T = 0, /* groups of g tokens of one channel ("per channel", K in KIVI) */
+    KVQ_GROUP_ALONG_C = 1  /* groups of g channels of one token ("per token", V in KIVI)  */
+} kvq_axis;
+
+typedef struct { int64_t outer, T, C; } kvq_shape;
+
+/* Quantized format.  Fields are plain ints so the layout is fixed.
+ *  bits        2, 4 or 8.
+ *  mode        KVQ_SYM: q = clip(rint(x/s), -qmax, qmax), s = max|x|/qmax
+ *              ([FtC] §1.1); qmin is ignored (treated as -qmax).
+ *              KVQ_ASYM: s = (max-min)/(qmax-qmin), zp = rint(qmin - min/s),
+ *              q = clip(rint(x/s) + zp, qmin, qmax) ([FtC] §1.2).
+ *  qmin, qmax  integer code range.  SYM: 1 <= qmax <= 2^(bits-1)-1.
+ *              ASYM: qmin < qmax, both in [-2^(bits-1), 2^(bits-1)-1] when
+ *              qmin < 0, else in [0, 2^bits - 1].
+ *  axis        grouping axis (kvq_axis).
+ *  group       g >= 1 elements per group; 0 = the whole axis (all quantized
+ *              tokens for ALONG_T, all C channels for ALONG_C).  A shorter
+ *              last group gets its own scale.
+ *  residual    R >= 0: the last min(R, T) tokens of every [outer] slice are
+ *              kept unquantized in the source dtype ([KVC] residual window).
+ *  scale_dtype KVQ_F32 or KVQ_BF16.
+ *  zero_dtype  KVQ_NONE for SYM; KVQ_I8 (saturating), KVQ_BF16 or KVQ_F32 for
+ *              ASYM.
+ * Arithmetic: float32 IEEE operations rounded to nearest-even, a true
+ * division, abs-max / range floored at the float32 value nearest 1e-8, and the
+ * codes computed from the scale and zero point AS STORED (bf16 metadata is
+ * rounded first). */
+typedef struct {
+    int32_t bits;
+    int32_t mode;
+    int32_t qmin;
+    int32_t qmax;
+    int32_t axis;
+    int64_t group;
+    int64_t residual;
+    int32_t scale_dtype;
+    int32_t zero_dtype;
+} kvq_qparams;
+
+/* [FtC] §1.3 error metrics, accumulated in binary64. */
+typedef struct { double rmse, max_abs, mean_abs; } kvq_err;
+
+/*
+ * Layout of the quantized representation (Tq = T - min(R, T) quantized tokens):
+ *  codes   uint8 [outer][Tq][C*bits/8]; element c of a token sits in byte
+ *          c*bits/8 at bit (c mod (8/bits))*bits, lowest bits first, holding
+ *          (q & (2^bits - 1)).  Codes are signed (two's complement) when
+ *          mode is SYM or qmin < 0, else unsigned.  C*bits must be a
+ *          multiple of 8.
+ *  scale   ALONG_T: [outer][ceil(Tq/g)][C];  ALONG_C: [outer][Tq][ceil(C/g)].
+ *  zero    same shape as scale (absent for SYM).
+ *  resid   [outer][min(R,T)][C] in the source dtype.
+ */
+
+/* Sizes in bytes of every buffer kvq_quantize writes, plus the workspace that
+ * kvq_quantize and kvq_error_stats need (one workspace of this size serves
+ * both).  [KVC] storage table: payload bits/8 per number plus per-group
+ * metadata.  Host only; no CUDA call.  Returns KVQ_EINVAL on a bad format. */
+KVQ_API kvq_status kvq_quantized_sizes(const kvq_shape* shape, kvq_dtype x_dtype, const kvq_qparams* p,
+                               size_t* codes_B, size_t* scale_B, size_t* zero_B,
+                               size_t* resid_B, size_t* workspace_B);
+
+/* Quantize x ([outer, T, C], KVQ_F32 or KVQ_BF16) into codes / scale / zero /
+ * resid ([FtC] §1.1, §1.2; [KVC] group-wise form, KIVI axes, residual).
+ * zero may be NULL for SYM and resid may be NULL when min(R,T) = 0.
+ * workspace may be NULL when kvq_quantized_sizes reported 0. */
+KVQ_API kvq_status kvq_quantize(const void* x, kvq_dtype x_dtype, const kvq_shape* shape,
+                        const kvq_qparams* p, void* codes, void* scale, void* zero, void* resid,
+                        void* workspace, size_t workspace_B, void* stream);
+
+/* x_hat = (q - zp) * s in float32, rounded once to out_dtype (KVQ_F32 or
+ * KVQ_BF16) ([FtC] §1.3); the residual tokens are copied back unchanged, so
+ * when R > 0 out_dtype must be the dtype the residual was stored in. */
+KVQ_API kvq_status kvq_dequantize(const void* codes, const void* scale, const void* zero, const void* resid,
+                          const kvq_shape* shape, const kvq_qparams* p,
+                          void* out, kvq_dtype out_dtype, void* stream);
+
+/* RMSE, max |x - x_hat| and mean |x - x_hat| over all N = outer*T*C elements
+ * ([FtC] §1.3), x_hat being what kvq_dequantize returns in x_dtype (residual
+ * tokens contribute zero error).  x_hat never goes to memory.  out_dev is a
+ * device pointer to one kvq_err.  N = 0 is KVQ_EINVAL. */
+KVQ_API kvq_status kvq_error_stats(const void* x, kvq_dtype x_dtype, const void* codes, const void* scale,
+                           const void* zero, const void* resid, const kvq_shape* shape,
+                           const kvq_qparams* p, kvq_err* out_dev,
+                           void* workspace, size_t workspace_B, void* stream);
+
+/* [FtC] §2: original bytes / (codes + scale + zero + residual bytes).  Host
+ * only.  Returns 0 when the denominator is 0. */
+KVQ_API double kvq_compression_ratio(size_t orig_B, size_t codes_B, size_t scale_B, size_t zero_B,
+                             size_t resid_B);
+
+/* [FtC] §4: total_tokens / kept_tokens into *out; KVQ_EINVAL unless
+ * 0 < kept_tokens <= total_tokens.  Host only. */
+KVQ_API kvq_status kvq_token_compression_ratio(int64_t total_tokens, int64_t kept_tokens, double* out);
+
+/* Workspace bytes for kv_h2o_select / kv_snapkv_select on [heads, *, T]. */
+KVQ_API kvq_status kv_select_workspace(int64_t heads, int64_t T, size_t* workspace_B);
+
+/* H2O keep set ([FtC] §3.1, §3.2).  hist: float32 [heads][steps][T] attention
+ * history.  Per head: score[i] = sum over t = 0..steps-1, in that order, of
+ * hist[t][i] (float32 adds); W' = min(window, T); the candidates are
+ * [0, T-W'); the k = min(budget-W', T-W') best by (score descending, index
+ * ascending) are unioned with the recent window [T-W', T).
+ * keep: int32 [heads][min(budget, T)], ascending.  scores: float32
+ * [heads][T] or NULL.  budget >= 1, 0 <= window <= budget, steps >= 1,
+ * T < 2^31; otherwise KVQ_EINVAL. */
+KVQ_API kvq_status kv_h2o_select(const float* hist, int64_t heads, int64_t steps, int64_t T,
+                         int64_t budget, int64_t window, int32_t* keep, float* scores,
+                         void* workspace, size_t workspace_B, void* stream);
+
+/* SnapKV keep set ([FtC] §3.3): as kv_h2o_select, with the observation score
+ * score[i] = (sum of the last obs_window rows, in order) / obs_window.
+ * 1 <= obs_window <= steps; steps = obs_window = 1 passes precomputed scores. */
+KVQ_API kvq_status kv_snapkv_select(const float* hist, int64_t heads, int64_t steps, int64_t T,
+                            int64_t obs_window, int64_t budget, int64_t window, int32_t* keep,
+                            float* scores, void* workspace, size_t workspace_B, void* stream);
+
+/* Compaction ([KVC] eviction frees the dropped entries):
+ * out[h][j][:] = kv[h][keep[h][j]][:] for j < K, kv [heads][T][D] of dtype
+ * (KVQ_F32, KVQ_BF16 or KVQ_I8 element size), keep int32 [heads][K],
+ * out [heads][K][D].  0 <= K <= T.  A keep entry outside [0, T) is not
+ * dereferenced: its output row is filled with zero bytes. */
+KVQ_API kvq_status kv_compact(const void* kv, kvq_dtype dtype, int64_t heads, int64_t T, int64_t D,
+                      const int32_t* keep, int64_t K, void* out, void* stream);
+
+/* Message describing the last non-OK status returned on this thread. */
+KVQ_API const char* kvq_last_error(void);
+
+/* Library version string. */
+KVQ_API const char* kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

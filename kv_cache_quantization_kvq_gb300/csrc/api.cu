@@ -1,0 +1,360 @@
+// api.cu -- the extern "C" entry points declared in include/kvq.h.
+//
+// Every argument is validated here, on the host, before anything is
+// launched; a rejected call has no side effect.  The size queries and the
+// ratio helpers never touch the CUDA runtime.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <algorithm>
+#include <string>
+
+#include "kvq_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvq_status fail(kvq_status s, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+kvq_status cuda_status(cudaError_t e, const char* what)
+{
+    if (e == cudaSuccess) return KVQ_OK;
+    return fail(KVQ_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int64_t kMaxElems = int64_t(1) << 50;   // keeps every index product in int64
+
+bool mul_ok(int64_t a, int64_t b, int64_t c)
+{
+    if (a == 0 || b == 0 || c == 0) return true;
+    return a <= kMaxElems / b && a * b <= kMaxElems / c;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Typed accesses need natural alignment; workspaces hold 32/64-bit atomics
+// and partial sums.  Misaligned buffers are rejected before any launch.
+kvq_status need_align(const void* p, size_t a, const char* name)
+{
+    if (p && a > 1 && ((uintptr_t)p % a) != 0) return fail(KVQ_EINVAL, "%s must be %zu-byte aligned", name, a);
+    return KVQ_OK;
+}
+
+size_t dtype_bytes(int dt)
+{
+    switch (dt) {
+    case KVQ_F32: return 4;
+    case KVQ_BF16: return 2;
+    case KVQ_I8: return 1;
+    default: return 0;
+    }
+}
+
+// Validate a format over a shape and derive the kernel-side description.
+kvq_status make_spec(const kvq_shape* sh, int x_dt, const kvq_qparams* p, kvq::QSpec& q)
+{
+    if (!sh || !p) return fail(KVQ_EINVAL, "shape and qparams must not be NULL");
+    if (sh->outer < 0 || sh->T < 0 || sh->C < 0) return fail(KVQ_EINVAL, "negative extent");
+    if (!mul_ok(sh->outer, sh->T, sh->C)) return fail(KVQ_EINVAL, "tensor too large");
+    if (x_dt != KVQ_F32 && x_dt != KVQ_BF16) return fail(KVQ_EINVAL, "source dtype must be F32 or BF16");
+    if (p->bits != 2 && p->bits != 4 && p->bits != 8) return fail(KVQ_EINVAL, "bits must be 2, 4 or 8 (got %d)", p->bits);
+    if ((sh->C * p->bits) % 8 != 0) return fail(KVQ_EINVAL, "C*bits must be a multiple of 8");
+    if (p->axis != KVQ_GROUP_ALONG_T && p->axis != KVQ_GROUP_ALONG_C) return fail(KVQ_EINVAL, "bad axis");
+    if (p->group < 0 || p->residual < 0) return fail(KVQ_EINVAL, "group and residual must be >= 0");
+    if (p->scale_dtype != KVQ_F32 && p->scale_dtype != KVQ_BF16) return fail(KVQ_EINVAL, "scale dtype must be F32 or BF16");
+    const int half = 1 << (p->bits - 1);
+    if (p->mode == KVQ_SYM) {
+        if (p->qmax < 1 || p->qmax > half - 1) return fail(KVQ_EINVAL, "symmetric qmax must be in [1, %d]", half - 1);
+        if (p->zero_dtype != KVQ_NONE) return fail(KVQ_EINVAL, "symmetric formats store no zero point (zero_dtype NONE)");
+    } else if (p->mode == KVQ_ASYM) {
+        if (p->qmin >= p->qmax) return fail(KVQ_EINVAL, "qmin must be < qmax");
+        if (p->qmin < 0) {
+            if (p->qmin < -half || p->qmax > half - 1) return fail(KVQ_EINVAL, "signed code range does not fit %d bits", p->bits);
+        } else if (p->qmax > (1 << p->bits) - 1) {
+            return fail(KVQ_EINVAL, "unsigned code range does not fit %d bits", p->bits);
+        }
+        if (p->zero_dtype != KVQ_I8 && p->zero_dtype != KVQ_BF16 && p->zero_dtype != KVQ_F32)
+            return fail(KVQ_EINVAL, "asymmetric zero dtype must be I8, BF16 or F32");
+    } else {
+        return fail(KVQ_EINVAL, "bad mode");
+    }
+    q.outer = sh->outer;
+    q.T = sh->T;
+    q.C = sh->C;
+    q.R = std::min(p->residual, sh->T);
+    q.Tq = sh->T - q.R;
+    q.g = p->group > 0 ? p->group : (p->axis == KVQ_GROUP_ALONG_T ? q.Tq : q.C);
+    if (q.g < 1) q.g = 1;
+    q.ngroups = p->axis == KVQ_GROUP_ALONG_T ? (q.Tq + q.g - 1) / q.g : (q.C + q.g - 1) / q.g;
+    q.bits = p->bits;
+    q.mode = p->mode;
+    q.axis = p->axis;
+    q.qmax = p->qmax;
+    q.qmin = p->mode == KVQ_SYM ? -p->qmax : p->qmin;
+    q.x_dt = x_dt;
+    q.scale_dt = p->scale_dtype;
+    q.zero_dt = p->mode == KVQ_SYM ? KVQ_NONE : p->zero_dtype;
+    q.is_signed = (p->mode == KVQ_SYM || p->qmin < 0) ? 1 : 0;
+    q.lo = (float)q.qmin;
+    q.hi = (float)q.qmax;
+    q.aligned = 1;
+    return KVQ_OK;
+}
+
+struct Sizes { size_t codes, scale, zero, resid; };
+
+Sizes sizes_of(const kvq::QSpec& q)
+{
+    Sizes s;
+    int64_t ng = 0;
+    if (q.outer > 0 && q.Tq > 0 && q.C > 0)
+        ng = q.axis == KVQ_GROUP_ALONG_T ? q.outer * q.ngroups * q.C : q.outer * q.Tq * q.ngroups;
+    s.codes = (size_t)(q.outer * q.Tq * q.C * q.bits / 8);
+    s.scale = (size_t)ng * dtype_bytes(q.scale_dt);
+    s.zero = q.mode == KVQ_ASYM ? (size_t)ng * dtype_bytes(q.zero_dt) : 0;
+    s.resid = (size_t)(q.outer * q.R * q.C) * dtype_bytes(q.x_dt);
+    return s;
+}
+
+size_t workspace_of(kvq::QSpec q)
+{
+    // the launch geometry depends on buffer alignment, unknown here: take the
+    // larger of the aligned and unaligned requirements
+    q.aligned = 1;
+    size_t w = std::max(kvq::quantize_workspace(q), kvq::errstats_workspace(q));
+    q.aligned = 0;
+    w = std::max(w, std::max(kvq::quantize_workspace(q), kvq::errstats_workspace(q)));
+    return w;
+}
+
+kvq_status need_ptr(const void* p, size_t bytes, const char* name)
+{
+    if (bytes > 0 && !p) return fail(KVQ_EINVAL, "%s must not be NULL", name);
+    return KVQ_OK;
+}
+
+}  // namespace
+
+namespace kvq {
+
+bool along_c_fast_ok(const QSpec& q)
+{
+    if (!q.aligned || q.C % 8 != 0 || q.g % 8 != 0 || q.C % q.g != 0 || q.g / 8 > 32) return false;
+    const int64_t cpr = q.C / 8;
+    return (cpr & (cpr - 1)) == 0;
+}
+
+bool along_t_fast_ok(const QSpec& q) { return q.aligned && q.C % 8 == 0; }
+
+int sm_count()
+{
+    static int cache[128] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 148;
+    }
+    return cache[dev];
+}
+
+}  // namespace kvq
+
+extern "C" {
+
+const char* kvq_last_error(void) { return g_last_error.c_str(); }
+
+const char* kvq_version(void) { return "kvq 0.1.0 (sm_103a)"; }
+
+kvq_status kvq_quantized_sizes(const kvq_shape* shape, kvq_dtype x_dtype, const kvq_qparams* p,
+                               size_t* codes_B, size_t* scale_B, size_t* zero_B, size_t* resid_B,
+                               size_t* workspace_B)
+{
+    kvq::QSpec q;
+    kvq_status s = make_spec(shape, x_dtype, p, q);
+    if (s != KVQ_OK) return s;
+    const Sizes z = sizes_of(q);
+    if (codes_B) *codes_B = z.codes;
+    if (scale_B) *scale_B = z.scale;
+    if (zero_B) *zero_B = z.zero;
+    if (resid_B) *resid_B = z.resid;
+    if (workspace_B) *workspace_B = workspace_of(q);
+    return KVQ_OK;
+}
+
+kvq_status kvq_quantize(const void* x, kvq_dtype x_dtype, const kvq_shape* shape, const kvq_qparams* p,
+                        void* codes, void* scale, void* zero, void* resid, void* workspace,
+                        size_t workspace_B, void* stream)
+{
+    kvq::QSpec q;
+    kvq_status s = make_spec(shape, x_dtype, p, q);
+    if (s != KVQ_OK) return s;
+    const Sizes z = sizes_of(q);
+    const size_t xB = (size_t)(q.outer * q.T * q.C) * dtype_bytes(x_dtype);
+    if ((s = need_ptr(x, xB, "x")) || (s = need_ptr(codes, z.codes, "codes")) ||
+        (s = need_ptr(scale, z.scale, "scale")) || (s = need_ptr(zero, z.zero, "zero")) ||
+        (s = need_ptr(resid, z.resid, "resid")))
+        return s;
+    if ((s = need_align(x, dtype_bytes(x_dtype), "x")) || (s = need_align(resid, dtype_bytes(x_dtype), "resid")) ||
+        (s = need_align(scale, dtype_bytes(q.scale_dt), "scale")) ||
+        (s = need_align(zero, dtype_bytes(q.zero_dt), "zero")) || (s = need_align(workspace, 16, "workspace")))
+        return s;
+    q.aligned = aligned16(x) && aligned16(codes) && aligned16(resid) && aligned16(scale) && aligned16(zero);
+    const size_t need = kvq::quantize_workspace(q);
+    if (need > 0 && (!workspace || workspace_B < need))
+        return fail(KVQ_EWORKSPACE, "kvq_quantize needs %zu workspace bytes (got %zu)", need, workspace_B);
+    kvq::QArgs a = {x, codes, scale, zero, resid, nullptr, workspace, workspace_B, q};
+    return cuda_status(kvq::launch_quantize(a, (cudaStream_t)stream), "kvq_quantize launch");
+}
+
+kvq_status kvq_dequantize(const void* codes, const void* scale, const void* zero, const void* resid,
+                          const kvq_shape* shape, const kvq_qparams* p, void* out, kvq_dtype out_dtype,
+                          void* stream)
+{
+    kvq::QSpec q;
+    kvq_status s = make_spec(shape, out_dtype, p, q);
+    if (s != KVQ_OK) return s;
+    const Sizes z = sizes_of(q);
+    const size_t oB = (size_t)(q.outer * q.T * q.C) * dtype_bytes(out_dtype);
+    if ((s = need_ptr(out, oB, "out")) || (s = need_ptr(codes, z.codes, "codes")) ||
+        (s = need_ptr(scale, z.scale, "scale")) || (s = need_ptr(zero, z.zero, "zero")) ||
+        (s = need_ptr(resid, z.resid, "resid")))
+        return s;
+    if ((s = need_align(out, dtype_bytes(out_dtype), "out")) || (s = need_align(resid, dtype_bytes(out_dtype), "resid")) ||
+        (s = need_align(scale, dtype_bytes(q.scale_dt), "scale")) || (s = need_align(zero, dtype_bytes(q.zero_dt), "zero")))
+        return s;
+    q.aligned = aligned16(out) && aligned16(codes) && aligned16(resid) && aligned16(scale) && aligned16(zero);
+    kvq::QArgs a = {nullptr, const_cast<void*>(codes), const_cast<void*>(scale), const_cast<void*>(zero),
+                    const_cast<void*>(resid), out, nullptr, 0, q};
+    return cuda_status(kvq::launch_dequantize(a, out_dtype, (cudaStream_t)stream), "kvq_dequantize launch");
+}
+
+kvq_status kvq_error_stats(const void* x, kvq_dtype x_dtype, const void* codes, const void* scale,
+                           const void* zero, const void* resid, const kvq_shape* shape, const kvq_qparams* p,
+                           kvq_err* out_dev, void* workspace, size_t workspace_B, void* stream)
+{
+    kvq::QSpec q;
+    kvq_status s = make_spec(shape, x_dtype, p, q);
+    if (s != KVQ_OK) return s;
+    if (q.outer * q.T * q.C == 0) return fail(KVQ_EINVAL, "error statistics of an empty tensor are undefined");
+    const Sizes z = sizes_of(q);
+    const size_t xB = (size_t)(q.outer * q.T * q.C) * dtype_bytes(x_dtype);
+    if ((s = need_ptr(x, xB, "x")) || (s = need_ptr(codes, z.codes, "codes")) ||
+        (s = need_ptr(scale, z.scale, "scale")) || (s = need_ptr(zero, z.zero, "zero")) ||
+        (s = need_ptr(out_dev, 1, "out_dev")))
+        return s;
+    if ((s = need_align(x, dtype_bytes(x_dtype), "x")) || (s = need_align(scale, dtype_bytes(q.scale_dt), "scale")) ||
+        (s = need_align(zero, dtype_bytes(q.zero_dt), "zero")) || (s = need_align(out_dev, 8, "out_dev")) ||
+        (s = need_align(workspace, 16, "workspace")))
+        return s;
+    (void)resid;   // residual tokens are exact by construction: not read
+    q.aligned = aligned16(x) && aligned16(codes) && aligned16(scale) && aligned16(zero);
+    const size_t need = kvq::errstats_workspace(q);
+    if (!workspace || workspace_B < need)
+        return fail(KVQ_EWORKSPACE, "kvq_error_stats needs %zu workspace bytes (got %zu)", need, workspace_B);
+    kvq::QArgs a = {x, const_cast<void*>(codes), const_cast<void*>(scale), const_cast<void*>(zero),
+                    const_cast<void*>(resid), nullptr, workspace, workspace_B, q};
+    return cuda_status(kvq::launch_error_stats(a, out_dev, (cudaStream_t)stream), "kvq_error_stats launch");
+}
+
+double kvq_compression_ratio(size_t orig_B, size_t codes_B, size_t scale_B, size_t zero_B, size_t resid_B)
+{
+    const double d = (double)codes_B + (double)scale_B + (double)zero_B + (double)resid_B;
+    return d > 0 ? (double)orig_B / d : 0.0;
+}
+
+kvq_status kvq_token_compression_ratio(int64_t total_tokens, int64_t kept_tokens, double* out)
+{
+    if (!out) return fail(KVQ_EINVAL, "out must not be NULL");
+    if (total_tokens <= 0 || kept_tokens <= 0 || kept_tokens > total_tokens)
+        return fail(KVQ_EINVAL, "require 0 < kept_tokens <= total_tokens");
+    *out = (double)total_tokens / (double)kept_tokens;
+    return KVQ_OK;
+}
+
+kvq_status kv_select_workspace(int64_t heads, int64_t T, size_t* workspace_B)
+{
+    if (!workspace_B) return fail(KVQ_EINVAL, "workspace_B must not be NULL");
+    if (heads < 0 || T < 0 || T > INT32_MAX || !mul_ok(heads, T, 1)) return fail(KVQ_EINVAL, "bad heads / T");
+    *workspace_B = kvq::select_workspace(heads, T);
+    return KVQ_OK;
+}
+
+static kvq_status select_common(const float* hist, int64_t heads, int64_t steps, int64_t T, int64_t obs,
+                                bool snap, int64_t budget, int64_t window, int32_t* keep, float* scores,
+                                void* workspace, size_t workspace_B, void* stream)
+{
+    if (heads < 0 || T < 0 || T > INT32_MAX) return fail(KVQ_EINVAL, "bad heads / T");
+    if (steps < 1) return fail(KVQ_EINVAL, "steps must be >= 1");
+    if (!mul_ok(heads, steps, T)) return fail(KVQ_EINVAL, "history too large");
+    if (budget < 1) return fail(KVQ_EINVAL, "budget must be >= 1");
+    if (window < 0 || window > budget) return fail(KVQ_EINVAL, "window must be in [0, budget]");
+    if (snap && (obs < 1 || obs > steps)) return fail(KVQ_EINVAL, "obs_window must be in [1, steps]");
+    kvq_status s;
+    const int64_t K = std::min(budget, T);
+    if ((s = need_ptr(hist, (size_t)(heads * steps * T), "hist")) || (s = need_ptr(keep, (size_t)(heads * K), "keep")))
+        return s;
+    if ((s = need_align(hist, 4, "hist")) || (s = need_align(keep, 4, "keep")) || (s = need_align(scores, 4, "scores")) ||
+        (s = need_align(workspace, 16, "workspace")))
+        return s;
+    const size_t need = kvq::select_workspace(heads, T);
+    if (heads * T > 0 && (!workspace || workspace_B < need))
+        return fail(KVQ_EWORKSPACE, "selection needs %zu workspace bytes (got %zu)", need, workspace_B);
+    kvq::SelectArgs a;
+    a.hist = hist;
+    a.heads = heads;
+    a.steps = steps;
+    a.T = T;
+    a.row0 = snap ? steps - obs : 0;
+    a.nrows = snap ? obs : steps;
+    a.divide = snap ? 1 : 0;
+    a.budget = budget;
+    a.window = window;
+    a.keep = keep;
+    a.scores = scores;
+    a.ws = workspace;
+    a.ws_B = workspace_B;
+    return cuda_status(kvq::launch_select(a, (cudaStream_t)stream), snap ? "kv_snapkv_select launch" : "kv_h2o_select launch");
+}
+
+kvq_status kv_h2o_select(const float* hist, int64_t heads, int64_t steps, int64_t T, int64_t budget, int64_t window,
+                         int32_t* keep, float* scores, void* workspace, size_t workspace_B, void* stream)
+{
+    return select_common(hist, heads, steps, T, steps, false, budget, window, keep, scores, workspace, workspace_B, stream);
+}
+
+kvq_status kv_snapkv_select(const float* hist, int64_t heads, int64_t steps, int64_t T, int64_t obs_window,
+                            int64_t budget, int64_t window, int32_t* keep, float* scores, void* workspace,
+                            size_t workspace_B, void* stream)
+{
+    return select_common(hist, heads, steps, T, obs_window, true, budget, window, keep, scores, workspace,
+                         workspace_B, stream);
+}
+
+kvq_status kv_compact(const void* kv, kvq_dtype dtype, int64_t heads, int64_t T, int64_t D, const int32_t* keep,
+                      int64_t K, void* out, void* stream)
+{
+    const size_t es = dtype_bytes(dtype);
+    if (es == 0) return fail(KVQ_EINVAL, "dtype must be F32, BF16 or I8");
+    if (heads < 0 || T < 0 || D < 0 || T > INT32_MAX || !mul_ok(heads, T, D)) return fail(KVQ_EINVAL, "bad extents");
+    if (K < 0 || K > T) return fail(KVQ_EINVAL, "require 0 <= K <= T");
+    kvq_status s;
+    if ((s = need_ptr(kv, (size_t)(heads * T * D), "kv")) || (s = need_ptr(keep, (size_t)(heads * K), "keep")) ||
+        (s = need_ptr(out, (size_t)(heads * K * D), "out")))
+        return s;
+    if ((s = need_align(keep, 4, "keep"))) return s;
+    return cuda_status(kvq::launch_compact(kv, es, heads, T, D, keep, K, out, (cudaStream_t)stream), "kv_compact launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// kvq_internal.h -- internal interface between the C-ABI layer (api.cu) and
+// the kernel launchers.  Not installed; callers use include/kvq.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+// Validated, derived description of one quantized format over [outer, T, C].
+struct QSpec {
+    int64_t outer, T, C;
+    int64_t Tq;       // quantized tokens = T - R
+    int64_t R;        // residual tokens  = min(residual, T)
+    int64_t g;        // effective group length (>= 1)
+    int64_t ngroups;  // ALONG_T: ceil(Tq/g) groups per channel; ALONG_C: ceil(C/g) per token
+    int32_t bits, mode, axis, qmin, qmax;  // SYM: qmin = -qmax
+    int32_t x_dt, scale_dt, zero_dt;
+    int32_t is_signed;                      // codes are two's complement
+    int32_t aligned;                        // all buffers 16-byte aligned
+    float lo, hi;                           // clip range as floats
+};
+
+struct QArgs {
+    const void* x;   // source [outer, T, C] (quantize, error stats)
+    void* codes;
+    void* scale;
+    void* zero;
+    void* resid;
+    void* out;       // dequantize output
+    void* ws;        // workspace
+    size_t ws_B;
+    QSpec q;
+};
+
+// ---- quantize / dequantize / error stats (quant.cu, dequant.cu, errstats.cu)
+size_t quantize_workspace(const QSpec& q);
+size_t errstats_workspace(const QSpec& q);
+cudaError_t launch_quantize(const QArgs& a, cudaStream_t st);
+cudaError_t launch_dequantize(const QArgs& a, int out_dt, cudaStream_t st);
+cudaError_t launch_error_stats(const QArgs& a, kvq_err* out_dev, cudaStream_t st);
+
+// Fast paths need 16-byte aligned buffers and these shapes; the generic
+// kernels handle everything else.
+bool along_c_fast_ok(const QSpec& q);
+bool along_t_fast_ok(const QSpec& q);
+
+// ---- keep-set selection (select.cu) and compaction (compact.cu)
+struct SelectArgs {
+    const float* hist;
+    int64_t heads, steps, T;
+    int64_t row0;      // first history row summed
+    int64_t nrows;     // rows summed (steps for H2O, obs_window for SnapKV)
+    int32_t divide;    // SnapKV: divide the sum by nrows
+    int64_t budget, window;
+    int32_t* keep;
+    float* scores;     // may be the workspace
+    void* ws;
+    size_t ws_B;
+};
+size_t select_workspace(int64_t heads, int64_t T);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
+
+cudaError_t launch_compact(const void* kv, size_t elem, int64_t heads, int64_t T, int64_t D,
+                           const int32_t* keep, int64_t K, void* out, cudaStream_t st);
+
+// number of SMs of the current device (cached per device)
+int sm_count();
+
+}  // namespace kvq

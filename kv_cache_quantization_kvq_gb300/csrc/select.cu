@@ -1,0 +1,382 @@
+// select.cu -- H2O / SnapKV keep-set selection.
+//
+// Method ("KV Compression 公式到源码对照" §3.1-§3.3):
+//   H2O score(i)    = sum over observed steps of a_t(i)   (float32, step order)
+//   SnapKV score(i) = (sum of the last w steps of a_t(i)) / w
+//   keep = TopK(score over [0, T-W'), B-W') union [T-W', T),  W' = min(W, T),
+//   ranked by (score descending, index ascending), written in ascending order.
+//
+// GPU design (one pass over the history from HBM, the rest from L2):
+//   colsum_hist   each thread owns 4 adjacent columns and walks the steps in
+//                 order (16-byte streaming loads), writes the scores and a
+//                 per-head histogram of the top 12 bits of an
+//                 order-preserving key of every candidate score.
+//   select_digit  per head: the bin holding the k-th largest key.
+//   refine_hist   histogram of the next digit among keys sharing the prefix
+//                 (12 bits, then the last 8): after three digits the k-th key
+//                 T* is exact, and so is the number of ties `need` to keep.
+//   count_chunks  per 1024-column chunk: keys > T* and keys == T*.
+//   emit          per chunk: offsets from the preceding chunks' counts, a
+//                 block scan for the tie ranks (lowest indices win), a block
+//                 scan for output positions; heavy hitters land sorted by
+//                 index, followed by the recent window.  No sort is needed:
+//                 scanning the kept flags in index order yields sorted output.
+#include <algorithm>
+
+#include "kvq_device.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kCols = 4 * kThreads;    // columns per chunk
+constexpr int kBins1 = 4096, kBins2 = 4096, kBins3 = 256;
+
+struct SelectLayout {
+    size_t scores, hist1, hist2, hist3, state, counts, total;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+SelectLayout layout(int64_t heads, int64_t T)
+{
+    SelectLayout L;
+    const int64_t nchunks = (T + kCols - 1) / kCols;
+    size_t off = 0;
+    L.scores = off; off = align256(off + (size_t)(heads * T) * 4);
+    L.hist1 = off;  off = align256(off + (size_t)heads * kBins1 * 4);
+    L.hist2 = off;  off = align256(off + (size_t)heads * kBins2 * 4);
+    L.hist3 = off;  off = align256(off + (size_t)heads * kBins3 * 4);
+    L.state = off;  off = align256(off + (size_t)heads * 4 * 4);
+    L.counts = off; off = align256(off + (size_t)(heads * nchunks) * 2 * 4);
+    L.total = off;
+    return L;
+}
+
+// candidate key: -0 folded onto +0 so that equal scores tie
+__device__ __forceinline__ uint32_t score_key(float s) { return float_key(s == 0.0f ? 0.0f : s); }
+
+// ---------------------------------------------------------------- scores
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads)
+colsum_hist_kernel(const SelectArgs a, int64_t rs, float* scores, uint32_t* hist1)
+{
+    __shared__ uint32_t sh[kBins1];
+    for (int i = threadIdx.x; i < kBins1; i += kThreads) sh[i] = 0;
+    __syncthreads();
+    const int64_t h = blockIdx.y;
+    const int64_t T = a.T;
+    const int64_t col0 = (int64_t)blockIdx.x * kCols + threadIdx.x * 4;
+    const float* base = a.hist + (h * a.steps + a.row0) * T;
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int64_t nr = a.nrows;
+    if (VEC) {
+        if (col0 < T) {
+            const float4* p = reinterpret_cast<const float4*>(base + col0);
+            const int64_t rstride = T / 4;
+            int64_t t = 0;
+            for (; t + 8 <= nr; t += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = __ldcs(p + (t + u) * rstride);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    s[0] = __fadd_rn(s[0], v[u].x);
+                    s[1] = __fadd_rn(s[1], v[u].y);
+                    s[2] = __fadd_rn(s[2], v[u].z);
+                    s[3] = __fadd_rn(s[3], v[u].w);
+                }
+            }
+            for (; t < nr; ++t) {
+                const float4 v = __ldcs(p + t * rstride);
+                s[0] = __fadd_rn(s[0], v.x);
+                s[1] = __fadd_rn(s[1], v.y);
+                s[2] = __fadd_rn(s[2], v.z);
+                s[3] = __fadd_rn(s[3], v.w);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t col = col0 + j;
+            if (col < T)
+                for (int64_t t = 0; t < nr; ++t) s[j] = __fadd_rn(s[j], base[t * T + col]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (a.divide) s[j] = __fdiv_rn(s[j], (float)nr);
+        const int64_t col = col0 + j;
+        if (col < T) {
+            if (!VEC) scores[h * T + col] = s[j];
+            if (col < rs) atomicAdd(&sh[score_key(s[j]) >> 20], 1u);
+        }
+    }
+    if (VEC && col0 < T) *reinterpret_cast<float4*>(scores + h * T + col0) = make_float4(s[0], s[1], s[2], s[3]);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kBins1; i += kThreads)
+        if (sh[i]) atomicAdd(&hist1[h * kBins1 + i], sh[i]);
+}
+
+// ---------------------------------------------------------------- block scans
+
+// exclusive prefix sum over the 256 threads of a block, in thread order
+__device__ __forceinline__ int block_excl_scan(int v, int& total)
+{
+    __shared__ int ws[kThreads / 32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) ws[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int y = lane < kThreads / 32 ? ws[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < kThreads / 32; o <<= 1) {
+            const int z = __shfl_up_sync(0xFFFFFFFFu, y, o);
+            if (lane >= o) y += z;
+        }
+        if (lane < kThreads / 32) ws[lane] = y;
+    }
+    __syncthreads();
+    const int incl = x + (w > 0 ? ws[w - 1] : 0);
+    total = ws[kThreads / 32 - 1];
+    __syncthreads();
+    return incl - v;
+}
+
+// ---------------------------------------------------------------- radix select
+
+// State per head: [0] key prefix so far, [1] rank still to find within it.
+// Finds, from the top bin down, the bin where the running count reaches r.
+__global__ void __launch_bounds__(1024)
+select_digit_kernel(const uint32_t* hist, int nbins, int digit_bits, int level, int64_t k,
+                    uint32_t* state)
+{
+    __shared__ int wsum[32];
+    __shared__ uint32_t s_prefix;
+    __shared__ int64_t s_r;
+    const int64_t h = blockIdx.x;
+    if (threadIdx.x == 0) {
+        s_prefix = level == 1 ? 0u : state[h * 4 + 0];
+        s_r = level == 1 ? k : (int64_t)state[h * 4 + 1];
+    }
+    __syncthreads();
+    const uint32_t* hb = hist + h * nbins;
+    const int bpt = (nbins + 1023) / 1024;                 // bins per thread (from the top)
+    const int top = nbins - 1 - threadIdx.x * bpt;         // this thread's highest bin
+    int local = 0;
+    for (int j = 0; j < bpt; ++j)
+        if (top - j >= 0) local += (int)hb[top - j];
+    // inclusive scan in thread order (= descending bins)
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int y = wsum[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+            const int z = __shfl_up_sync(0xFFFFFFFFu, y, o);
+            if (lane >= o) y += z;
+        }
+        wsum[lane] = y;
+    }
+    __syncthreads();
+    const int64_t incl = x + (w > 0 ? wsum[w - 1] : 0);
+    const int64_t excl = incl - local;
+    const int64_t r = s_r;
+    if (excl < r && r <= incl) {
+        int64_t acc = excl;
+        for (int j = 0; j < bpt; ++j) {
+            const int b = top - j;
+            if (b < 0) break;
+            if (acc + hb[b] >= r) {
+                state[h * 4 + 0] = (s_prefix << digit_bits) | (uint32_t)b;
+                state[h * 4 + 1] = (uint32_t)(r - acc);
+                break;
+            }
+            acc += hb[b];
+        }
+    }
+}
+
+// Histogram of the next digit among candidate keys matching the prefix.
+__global__ void __launch_bounds__(kThreads)
+refine_hist_kernel(const float* scores, int64_t T, int64_t rs, const uint32_t* state, int level,
+                   uint32_t* hist)
+{
+    __shared__ uint32_t sh[kBins2];
+    const int nbins = level == 2 ? kBins2 : kBins3;
+    for (int i = threadIdx.x; i < nbins; i += kThreads) sh[i] = 0;
+    __syncthreads();
+    const int64_t h = blockIdx.y;
+    const uint32_t prefix = state[h * 4 + 0];
+    const int64_t col0 = (int64_t)blockIdx.x * kCols + threadIdx.x * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int64_t col = col0 + j;
+        if (col < rs) {
+            const uint32_t key = score_key(scores[h * T + col]);
+            if (level == 2) { if ((key >> 20) == prefix) atomicAdd(&sh[(key >> 8) & 0xFFFu], 1u); }
+            else if ((key >> 8) == prefix) atomicAdd(&sh[key & 0xFFu], 1u);
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nbins; i += kThreads)
+        if (sh[i]) atomicAdd(&hist[h * nbins + i], sh[i]);
+}
+
+// Per chunk: candidates with key > T* and key == T*.
+__global__ void __launch_bounds__(kThreads)
+count_chunks_kernel(const float* scores, int64_t T, int64_t rs, const uint32_t* state, int32_t* counts)
+{
+    const int64_t h = blockIdx.y;
+    const uint32_t kth = state[h * 4 + 0];
+    const int64_t col0 = (int64_t)blockIdx.x * kCols + threadIdx.x * 4;
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int64_t col = col0 + j;
+        if (col < rs) {
+            const uint32_t key = score_key(scores[h * T + col]);
+            gt += key > kth;
+            eq += key == kth;
+        }
+    }
+    int tg, te;
+    block_excl_scan(gt, tg);
+    block_excl_scan(eq, te);
+    if (threadIdx.x == 0) {
+        counts[(h * gridDim.x + blockIdx.x) * 2 + 0] = tg;
+        counts[(h * gridDim.x + blockIdx.x) * 2 + 1] = te;
+    }
+}
+
+// mode 0: no heavy hitters (k = 0); 1: every candidate (k = T - W'); 2: threshold.
+__global__ void __launch_bounds__(kThreads)
+emit_kernel(const float* scores, int64_t T, int64_t rs, int64_t K, int64_t k, int mode,
+            const uint32_t* state, const int32_t* counts, int32_t* keep)
+{
+    __shared__ int64_t s_gt_before, s_eq_before;
+    const int64_t h = blockIdx.y;
+    const int64_t chunk = blockIdx.x;
+    const int64_t col0 = chunk * kCols + threadIdx.x * 4;
+    int32_t* kh = keep + h * K;
+
+    // the recent window: [rs, T) lands after the k heavy hitters
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int64_t col = col0 + j;
+        if (col >= rs && col < T) kh[k + (col - rs)] = (int32_t)col;
+    }
+    if (mode == 0) return;
+    if (mode == 1) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t col = col0 + j;
+            if (col < rs) kh[col] = (int32_t)col;
+        }
+        return;
+    }
+    if (chunk * kCols >= rs) return;                      // no candidates in this chunk (uniform)
+
+    if (threadIdx.x < 32) {
+        int64_t g = 0, e = 0;
+        for (int64_t c = threadIdx.x; c < chunk; c += 32) {
+            g += counts[(h * gridDim.x + c) * 2 + 0];
+            e += counts[(h * gridDim.x + c) * 2 + 1];
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xFFFFFFFFu, g, o);
+            e += __shfl_xor_sync(0xFFFFFFFFu, e, o);
+        }
+        if (threadIdx.x == 0) { s_gt_before = g; s_eq_before = e; }
+    }
+    __syncthreads();
+    const uint32_t kth = state[h * 4 + 0];
+    const int64_t need = (int64_t)state[h * 4 + 1];
+    uint32_t key[4];
+    bool cand[4];
+    int eq = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int64_t col = col0 + j;
+        cand[j] = col < rs;
+        key[j] = cand[j] ? score_key(scores[h * T + col]) : 0u;
+        eq += cand[j] && key[j] == kth;
+    }
+    int tot;
+    int64_t tie_rank = s_eq_before + block_excl_scan(eq, tot);
+    bool sel[4];
+    int nsel = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        sel[j] = false;
+        if (cand[j]) {
+            if (key[j] > kth) sel[j] = true;
+            else if (key[j] == kth) { sel[j] = tie_rank < need; ++tie_rank; }
+        }
+        nsel += sel[j];
+    }
+    int64_t pos = s_gt_before + min(s_eq_before, need) + block_excl_scan(nsel, tot);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (sel[j]) {
+            if (pos < k) kh[pos] = (int32_t)(col0 + j);   // never past the heavy-hitter slots
+            ++pos;
+        }
+}
+
+}  // namespace
+
+size_t select_workspace(int64_t heads, int64_t T) { return layout(heads, T).total; }
+
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st)
+{
+    const int64_t H = a.heads, T = a.T;
+    if (H == 0 || T == 0) return cudaSuccess;
+    const SelectLayout L = layout(H, T);
+    char* ws = static_cast<char*>(a.ws);
+    float* scores = a.scores ? a.scores : reinterpret_cast<float*>(ws + L.scores);
+    uint32_t* hist1 = reinterpret_cast<uint32_t*>(ws + L.hist1);
+    uint32_t* hist2 = reinterpret_cast<uint32_t*>(ws + L.hist2);
+    uint32_t* hist3 = reinterpret_cast<uint32_t*>(ws + L.hist3);
+    uint32_t* state = reinterpret_cast<uint32_t*>(ws + L.state);
+    int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+
+    const int64_t Wr = std::min(a.window, T);
+    const int64_t rs = T - Wr;
+    const int64_t k = std::min(a.budget - Wr, rs);
+    const int64_t K = std::min(a.budget, T);
+    const int mode = k == 0 ? 0 : (k == rs ? 1 : 2);
+    const int64_t nchunks = (T + kCols - 1) / kCols;
+    const dim3 grid((unsigned)nchunks, (unsigned)H);
+
+    cudaError_t e = cudaMemsetAsync(ws + L.hist1, 0, L.counts - L.hist1, st);
+    if (e != cudaSuccess) return e;
+    const bool vec = (T % 4 == 0) && ((uintptr_t)a.hist % 16 == 0) && ((uintptr_t)scores % 16 == 0);
+    if (vec) colsum_hist_kernel<true><<<grid, kThreads, 0, st>>>(a, rs, scores, hist1);
+    else colsum_hist_kernel<false><<<grid, kThreads, 0, st>>>(a, rs, scores, hist1);
+    if (mode == 2) {
+        select_digit_kernel<<<(unsigned)H, 1024, 0, st>>>(hist1, kBins1, 12, 1, k, state);
+        refine_hist_kernel<<<grid, kThreads, 0, st>>>(scores, T, rs, state, 2, hist2);
+        select_digit_kernel<<<(unsigned)H, 1024, 0, st>>>(hist2, kBins2, 12, 2, k, state);
+        refine_hist_kernel<<<grid, kThreads, 0, st>>>(scores, T, rs, state, 3, hist3);
+        select_digit_kernel<<<(unsigned)H, 1024, 0, st>>>(hist3, kBins3, 8, 3, k, state);
+        count_chunks_kernel<<<grid, kThreads, 0, st>>>(scores, T, rs, state, counts);
+    }
+    emit_kernel<<<grid, kThreads, 0, st>>>(scores, T, rs, K, k, mode, state, counts, a.keep);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,189 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+The library must load and export every entry point include/kvq.h declares;
+the host-only size / ratio functions must agree with the oracle; every
+argument check must reject bad input before anything reaches the GPU (the
+pages' ValueError cases and the documented contract).
+"""
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kb():
+    from kv_cache_quantization_kvq_gb300 import build
+    build()
+    from kv_cache_quantization_kvq_gb300 import binding
+    return binding
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "kvq.h")) as f:
+        src = f.read()
+    return set(re.findall(r"KVQ_API\s+[\w\s\*]+?\b(kvq?_\w+)\s*\(", src))
+
+
+def test_library_exports_every_declared_symbol(kb):
+    declared = declared_symbols()
+    assert len(declared) == 12
+    for name in declared:
+        assert hasattr(kb.LIB, name), name
+    assert declared == set(kb.EXPORTS)
+    assert kb.kvq_version().startswith("kvq ")
+
+
+def formats():
+    for bits in (8, 4, 2):
+        for axis in (0, 1):
+            for g in (0, 1, 8, 32, 64, 100):
+                for R in (0, 5, 1000):
+                    yield ("sym", bits, axis, g, R, O.F32, O.NONE)
+                    yield ("sym", bits, axis, g, R, O.BF16, O.NONE)
+                    yield ("asym", bits, axis, g, R, O.BF16, O.BF16)
+                    yield ("asym", bits, axis, g, R, O.F32, O.I8)
+
+
+def test_sizes_match_oracle(kb):
+    for (mode, bits, axis, g, R, sd, zd) in formats():
+        for shape in ((3, 77, 16), (1, 256, 128), (2, 0, 8), (0, 5, 8), (4, 9, 24)):
+            for xd in (O.F32, O.BF16):
+                if mode == "sym":
+                    oq = O.QParams.sym(bits, axis=axis, group=g, residual=R, scale_dtype=sd)
+                    kq = kb.QParams.sym(bits, axis=axis, group=g, residual=R, scale_dtype=sd)
+                else:
+                    qmin, qmax = (0, (1 << bits) - 1) if bits < 8 else (-128, 127)
+                    oq = O.QParams.asym(bits, qmin, qmax, axis=axis, group=g, residual=R, scale_dtype=sd, zero_dtype=zd)
+                    kq = kb.QParams.asym(bits, qmin, qmax, axis=axis, group=g, residual=R, scale_dtype=sd, zero_dtype=zd)
+                got = kb.kvq_quantized_sizes(shape, xd, kq)
+                assert got[:4] == O.sizes(shape, xd, oq), (shape, xd, kq)
+
+
+def test_compression_ratios_match_oracle(kb):
+    rng = np.random.default_rng(0)
+    for _ in range(100):
+        v = [int(a) for a in rng.integers(1, 1 << 40, 5)]
+        assert kb.kvq_compression_ratio(*v) == O.compression_ratio(*v)
+    assert kb.kvq_compression_ratio(10, 0, 0, 0, 0) == 0.0
+    assert kb.kvq_token_compression_ratio(131072, 2048) == 64.0
+    for bad in ((10, 0), (10, 11), (0, 0), (-3, 1)):
+        with pytest.raises(kb.KvqError) as e:
+            kb.kvq_token_compression_ratio(*bad)
+        assert e.value.status == kb.EINVAL
+
+
+def test_bad_formats_rejected(kb):
+    bad = [kb.QParams(3, kb.SYM, -3, 3),
+           kb.QParams.sym(4, qmax=8),
+           kb.QParams.sym(4, qmax=0),
+           kb.QParams.asym(4, 5, 5),
+           kb.QParams.asym(4, 0, 16),
+           kb.QParams.asym(4, -9, 7),
+           kb.QParams(4, kb.SYM, -7, 7, zero_dtype=kb.I8),
+           kb.QParams.asym(4, 0, 15, zero_dtype=kb.NONE),
+           kb.QParams.sym(4, scale_dtype=kb.I8),
+           kb.QParams(4, 7, 0, 7),
+           kb.QParams(4, kb.SYM, -7, 7, axis=5),
+           kb.QParams.sym(4, group=-1),
+           kb.QParams.sym(4, residual=-2)]
+    for qp in bad:
+        with pytest.raises(kb.KvqError) as e:
+            kb.kvq_quantized_sizes((1, 4, 8), kb.F32, qp)
+        assert e.value.status == kb.EINVAL, qp
+    for shape in ((1, 4, 3), (-1, 4, 8), (1 << 30, 1 << 30, 8)):
+        with pytest.raises(kb.KvqError):
+            kb.kvq_quantized_sizes(shape, kb.F32, kb.QParams.sym(4))
+    with pytest.raises(kb.KvqError):
+        kb.kvq_quantized_sizes((1, 4, 8), kb.I8, kb.QParams.sym(4))
+
+
+def test_calls_rejected_before_launch(kb):
+    """Every rejected call returns before touching the device: NULL buffers,
+    short workspaces, empty statistics, bad selection arguments."""
+    qp = kb.QParams.sym(4, axis=kb.ALONG_C, group=32)
+    shape = (2, 16, 64)
+    fake = 1 << 20  # never dereferenced: validation fails first
+    with pytest.raises(kb.KvqError) as e:
+        kb.kvq_quantize(None, kb.BF16, shape, qp, fake, fake, None, None, None, 0, 0)
+    assert e.value.status == kb.EINVAL and "x" in str(e.value)
+    with pytest.raises(kb.KvqError):
+        kb.kvq_quantize(fake, kb.BF16, shape, qp, None, fake, None, None, None, 0, 0)
+    with pytest.raises(kb.KvqError):       # residual window without a residual buffer
+        kb.kvq_quantize(fake, kb.BF16, shape, kb.QParams.sym(4, residual=4), fake, fake, None, None, None, 0, 0)
+    with pytest.raises(kb.KvqError):       # asymmetric without a zero buffer
+        kb.kvq_quantize(fake, kb.BF16, shape, kb.QParams.asym(4, 0, 15, zero_dtype=kb.BF16), fake, fake, None,
+                        None, None, 0, 0)
+    with pytest.raises(kb.KvqError) as e:  # long groups need the workspace
+        kb.kvq_quantize(fake * 16, kb.BF16, (1, 1024, 64), kb.QParams.sym(8, group=0), fake * 16, fake * 16,
+                        None, None, None, 0, 0)
+    assert e.value.status == kb.EWORKSPACE
+    with pytest.raises(kb.KvqError) as e:
+        kb.kvq_error_stats(fake, kb.BF16, fake, fake, None, None, (0, 16, 64), qp, fake, fake, 1 << 20, 0)
+    assert e.value.status == kb.EINVAL
+    with pytest.raises(kb.KvqError) as e:
+        kb.kvq_error_stats(fake, kb.BF16, fake, fake, None, None, shape, qp, fake, None, 0, 0)
+    assert e.value.status == kb.EWORKSPACE
+    with pytest.raises(kb.KvqError):
+        kb.kvq_dequantize(fake, fake, None, None, shape, qp, None, kb.BF16, 0)
+    with pytest.raises(kb.KvqError):
+        kb.kvq_dequantize(fake, fake, None, None, shape, qp, fake, kb.I8, 0)
+
+    ws = kb.kv_select_workspace(4, 100)
+    assert ws > 4 * 100 * 4
+    sel = dict(hist=fake, heads=4, steps=8, T=100, keep=fake, scores=None, workspace=fake, workspace_B=ws)
+    for budget, window in ((0, 0), (5, 6), (5, -1)):
+        with pytest.raises(kb.KvqError) as e:
+            kb.kv_h2o_select(budget=budget, window=window, stream=0, **sel)
+        assert e.value.status == kb.EINVAL
+    with pytest.raises(kb.KvqError):
+        kb.kv_h2o_select(fake, 4, 0, 100, 10, 2, fake, None, fake, ws, 0)          # steps < 1
+    for obs in (0, 9):
+        with pytest.raises(kb.KvqError):
+            kb.kv_snapkv_select(fake, 4, 8, 100, obs, 10, 2, fake, None, fake, ws, 0)
+    with pytest.raises(kb.KvqError) as e:
+        kb.kv_h2o_select(fake, 4, 8, 100, 10, 2, fake, None, fake, ws - 1, 0)
+    assert e.value.status == kb.EWORKSPACE
+    with pytest.raises(kb.KvqError):
+        kb.kv_h2o_select(None, 4, 8, 100, 10, 2, fake, None, fake, ws, 0)
+    with pytest.raises(kb.KvqError):
+        kb.kv_select_workspace(1, 1 << 32)
+    # compaction: K outside [0, T], bad dtype, NULL buffers
+    for K in (-1, 101):
+        with pytest.raises(kb.KvqError):
+            kb.kv_compact(fake, kb.BF16, 4, 100, 128, fake, K, fake, 0)
+    with pytest.raises(kb.KvqError):
+        kb.kv_compact(fake, kb.NONE, 4, 100, 128, fake, 10, fake, 0)
+    with pytest.raises(kb.KvqError):
+        kb.kv_compact(fake, kb.BF16, 4, 100, 128, None, 10, fake, 0)
+    assert "NULL" in kb.kvq_last_error()
+
+
+def test_misaligned_buffers_rejected(kb):
+    """Typed buffers must be aligned to their element size and workspaces to
+    16 bytes; otherwise the call is rejected on the host."""
+    base = 1 << 24
+    qp = kb.QParams.sym(8, axis=kb.ALONG_T, group=16)            # float32 scale
+    shape = (1, 32, 16)
+    with pytest.raises(kb.KvqError) as e:
+        kb.kvq_quantize(base, kb.F32, shape, qp, base, base + 2, None, None, None, 0, 0)
+    assert e.value.status == kb.EINVAL and "aligned" in str(e.value)
+    with pytest.raises(kb.KvqError):
+        kb.kvq_quantize(base + 2, kb.F32, shape, qp, base, base, None, None, None, 0, 0)
+    with pytest.raises(kb.KvqError):
+        kb.kvq_dequantize(base, base, None, None, shape, qp, base + 1, kb.BF16, 0)
+    with pytest.raises(kb.KvqError):
+        kb.kvq_error_stats(base, kb.F32, base, base, None, None, shape, qp, base + 4, base, 1 << 20, 0)
+    ws = kb.kv_select_workspace(2, 64)
+    with pytest.raises(kb.KvqError):
+        kb.kv_h2o_select(base + 2, 2, 4, 64, 8, 2, base, None, base, ws, 0)
+    with pytest.raises(kb.KvqError):
+        kb.kv_h2o_select(base, 2, 4, 64, 8, 2, base, None, base + 8, ws, 0)
+    with pytest.raises(kb.KvqError):
+        kb.kv_compact(base, kb.BF16, 2, 64, 8, base + 1, 4, base, 0)
