@@ -189,6 +189,34 @@ KVQ_API kvq_status kv_snapkv_select(const float* hist, int64_t heads, int64_t st
 KVQ_API kvq_status kv_compact(const void* kv, kvq_dtype dtype, int64_t heads, int64_t T, int64_t D,
                       const int32_t* keep, int64_t K, void* out, void* stream);
 
+/* Size of the library's fixed scratch array used by kvq_error_stats_noalloc. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (1 << 20)
+
+/* kvq_error_stats without a workspace argument.  The pages have no
+ * counterpart to this entry point: it exists for callers that cannot allocate
+ * device memory at the moment they need the statistics -- for example a
+ * serving loop whose memory pool already owns all device memory, or code that
+ * must not call cudaMalloc on its hot path because cudaMalloc may synchronise
+ * the device.  It computes exactly what kvq_error_stats computes, with the same
+ * arguments minus the workspace, and allocates nothing: the partial sums live
+ * in a fixed array of KVQ_NOALLOC_SCRATCH_BYTES (1 MiB) compiled into the
+ * library, which every GPU that loads the library keeps until the process
+ * exits.
+ *  - Limit: shapes whose partial sums need more than that array return
+ *    KVQ_EWORKSPACE (with a message) before anything is launched; use
+ *    kvq_error_stats with a workspace for them.
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress) with that device current; make that first
+ *    call before any stream capture.
+ *  - Sharing: every call uses the same array and it keeps the previous call's
+ *    contents (each call overwrites what it reads).  Calls that may overlap on
+ *    the GPU (other streams, other host threads) race on the array: order them
+ *    on one stream or synchronise between them. */
+KVQ_API kvq_status kvq_error_stats_noalloc(const void* x, kvq_dtype x_dtype, const void* codes,
+                                           const void* scale, const void* zero, const void* resid,
+                                           const kvq_shape* shape, const kvq_qparams* p, kvq_err* out_dev,
+                                           void* stream);
+
 /* Message describing the last non-OK status returned on this thread. */
 KVQ_API const char* kvq_last_error(void);
 

@@ -64,6 +64,7 @@ def _load() -> ctypes.CDLL:
         "kv_h2o_select": [vp, i64, i64, i64, i64, i64, vp, vp, vp, sz, vp],
         "kv_snapkv_select": [vp, i64, i64, i64, i64, i64, i64, vp, vp, vp, sz, vp],
         "kv_compact": [vp, i32, i64, i64, i64, vp, i64, vp, vp],
+        "kvq_error_stats_noalloc": [vp, i32, vp, vp, vp, vp, S, P, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -81,7 +82,11 @@ LIB = _load()
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_quantized_sizes", "kvq_quantize", "kvq_dequantize", "kvq_error_stats",
            "kvq_compression_ratio", "kvq_token_compression_ratio", "kv_select_workspace",
-           "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kvq_last_error", "kvq_version")
+           "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kvq_last_error", "kvq_version",
+           "kvq_error_stats_noalloc")
+
+# size of the library's fixed scratch array behind kvq_error_stats_noalloc
+NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 def _check(status: int):
@@ -170,6 +175,14 @@ def kvq_error_stats(x, x_dtype, codes, scale, zero, resid, shape, qp: QParams, o
     _check(LIB.kvq_error_stats(_ptr(x), x_dtype, _ptr(codes), _ptr(scale), _ptr(zero), _ptr(resid),
                                ctypes.byref(s), ctypes.byref(p), _ptr(out_dev), _ptr(workspace),
                                int(workspace_B), _stream(stream)))
+
+
+def kvq_error_stats_noalloc(x, x_dtype, codes, scale, zero, resid, shape, qp: QParams, out_dev, stream=None):
+    """kvq_error_stats for callers that cannot allocate: no workspace argument,
+    the library's fixed scratch array is used instead (see include/kvq.h)."""
+    s, p = _shape(shape), qp.c()
+    _check(LIB.kvq_error_stats_noalloc(_ptr(x), x_dtype, _ptr(codes), _ptr(scale), _ptr(zero), _ptr(resid),
+                                       ctypes.byref(s), ctypes.byref(p), _ptr(out_dev), _stream(stream)))
 
 
 def kvq_compression_ratio(orig_B, codes_B, scale_B, zero_B, resid_B) -> float:

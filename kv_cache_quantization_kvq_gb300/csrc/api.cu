@@ -156,6 +156,16 @@ bool along_c_fast_ok(const QSpec& q)
 
 bool along_t_fast_ok(const QSpec& q) { return q.aligned && q.C % 8 == 0; }
 
+void set_last_error(const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+}
+
 int sm_count()
 {
     static int cache[128] = {0};

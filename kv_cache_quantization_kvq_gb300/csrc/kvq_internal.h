@@ -70,4 +70,7 @@ cudaError_t launch_compact(const void* kv, size_t elem, int64_t heads, int64_t T
 // number of SMs of the current device (cached per device)
 int sm_count();
 
+// set the thread's kvq_last_error() message (printf-style)
+void set_last_error(const char* fmt, ...);
+
 }  // namespace kvq
