@@ -56,7 +56,6 @@ def kivi_bytes():
     meta = (outer * (Tq // g) * D) * 2 * 2          # K: bf16 scale + zero per (group, channel)
     meta_v = (outer * Tq * (D // g)) * 2 * 2        # V: per (token, group)
     resid = outer * R * D * 2
-    quant = 2 * x // 2 + (codes + meta + resid) + (codes + meta_v + resid)   # read x(K,V) + writes
     quant = x * 2 + codes * 2 + meta + meta_v + resid * 2
     dequant = quant                                                           # reverse direction
     stats = x * 2 + codes * 2 + meta + meta_v                                 # residual error is zero: not read
@@ -164,12 +163,20 @@ class ClockSampler:
 class Step:
     """Device buffers and the launches of one step, through the C ABI."""
 
-    def __init__(self, b, dev, stream):
+    def __init__(self, b, dev, stream, only="all"):
         import torch
         from kv_cache_quantization_kvq_gb300 import workloads as W
         self.b, self.dev, self.stream = b, dev, stream
         outer = KIVI["batch"] * KIVI["heads"]
         self.kshape = (outer, KIVI["T"], KIVI["D"])
+        if only in ("all", "kivi"):
+            self._init_kivi(b, dev, W)
+        if only in ("all", "evict"):
+            self._init_evict(b, dev, W)
+        torch.cuda.synchronize()
+
+    def _init_kivi(self, b, dev, W):
+        import torch
         self.K, self.V = W.kivi_kv(dev, seed=2, batch=KIVI["batch"], heads=KIVI["heads"], T=KIVI["T"], D=KIVI["D"])
         self.qpK = b.QParams.asym(4, 0, 15, axis=b.ALONG_T, group=KIVI["g"], residual=KIVI["R"],
                                   scale_dtype=b.BF16, zero_dtype=b.BF16)
@@ -181,6 +188,9 @@ class Step:
         self.dV = torch.empty_like(self.V)
         self.stK = torch.zeros(3, dtype=torch.float64, device=dev)
         self.stV = torch.zeros(3, dtype=torch.float64, device=dev)
+
+    def _init_evict(self, b, dev, W):
+        import torch
         H, S, T, D = EVICT["heads"], EVICT["steps"], EVICT["T"], EVICT["D"]
         self.hist, self.EK, self.EV = W.eviction_inputs(dev, seed=5, heads=H, steps=S, T=T, D=D,
                                                         window=EVICT["window"])
@@ -192,7 +202,6 @@ class Step:
         self.cV = torch.empty_like(self.cK)
         self.scK = torch.empty_like(self.cK)
         self.scV = torch.empty_like(self.cK)
-        torch.cuda.synchronize()
 
     # each phase returns the number of kernels it launched
     def quantize(self):
@@ -257,13 +266,15 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        st = Step(b, dev, stream)
+        st = Step(b, dev, stream, args.only)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
     kb, eb = kivi_bytes(), evict_bytes()
     pbytes = {**kb, **eb}
-    phases = list(Step.PHASES)
+    phases = [ph for ph in Step.PHASES
+              if args.only == "all" or (args.only == "kivi") == (ph in kb)]
+    pbytes = {ph: pbytes[ph] for ph in phases}
 
     def barrier():
         if world > 1:
@@ -304,17 +315,18 @@ def run_ours(args, rank, world, local_rank):
     total_bytes = sum(pbytes.values())
     value = world * total_bytes / (step_ms * 1e-3) / 1e9
 
-    # sanity of the step's outputs (not timed): selection sizes, finite stats
+    # sanity of the step's outputs (not timed): finite statistics
     torch.cuda.synchronize()
-    assert torch.isfinite(st.stK).all() and torch.isfinite(st.stV).all()
+    if "error_stats" in phases:
+        assert torch.isfinite(st.stK).all() and torch.isfinite(st.stV).all()
 
     result = None
     if rank == 0:
         peak, peak_kind = measured_peak()
-        h2o_ms = ph_ms["h2o_select"] + ph_ms["h2o_compact"]
+        h2o_ms = ph_ms.get("h2o_select", float("nan")) + ph_ms.get("h2o_compact", float("nan"))
         tokens = EVICT["heads"] * EVICT["T"]
-        sel_B = pbytes["h2o_select"]
-        sel_gbs = sel_B / (ph_ms["h2o_select"] * 1e-3) / 1e9
+        sel_B = evict_bytes()["h2o_select"]
+        sel_gbs = sel_B / (ph_ms["h2o_select"] * 1e-3) / 1e9 if "h2o_select" in ph_ms else float("nan")
         result = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
@@ -335,7 +347,9 @@ def run_ours(args, rank, world, local_rank):
             "wall_s_timed_region": round(wall, 3),
             "clocks": clk.summary(),
         }
-        if not args.no_e2e:
+        if args.only != "all":
+            result["config"]["only"] = args.only
+        if not args.no_e2e and args.only == "all":
             result["e2e"] = run_e2e(b, st, stream, dev, args, total_bytes, world)
         if not args.no_cpu_baseline and world == 1:
             result["cpu_baseline"] = cpu_baseline(min_seconds=args.cpu_seconds)
@@ -473,6 +487,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=("all", "kivi", "evict"), default="all",
+                    help="time only the KIVI phases or only the eviction phases (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

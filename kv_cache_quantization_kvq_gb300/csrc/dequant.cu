@@ -404,7 +404,8 @@ constexpr int kMaxSms = 1024;
 size_t errstats_workspace(const QSpec& q)
 {
     const Geometry G = geometry(q, kMaxSms);
-    return (size_t)G.grid.x * G.grid.y * sizeof(Partial);
+    const int64_t fast = fast_stats_blocks(q, kMaxSms);
+    return std::max<size_t>((size_t)G.grid.x * G.grid.y, (size_t)std::max<int64_t>(fast, 0)) * sizeof(Partial);
 }
 
 cudaError_t launch_dequantize(const QArgs& a, int out_dt, cudaStream_t st)
@@ -417,6 +418,7 @@ cudaError_t launch_dequantize(const QArgs& a, int out_dt, cudaStream_t st)
         copy_back_residual_kernel<<<(unsigned)g, 256, 0, st>>>(a, n, out_dt == KVQ_BF16 ? 2 : 4);
         return cudaGetLastError();
     }
+    if (fast_dequant_supported(q, out_dt)) return fast_dequantize(a, st);
     const Geometry G = geometry(q, sm_count());
     if (out_dt == KVQ_BF16) launch_bits<__nv_bfloat16, false>(a, G, nullptr, st);
     else launch_bits<float, false>(a, G, nullptr, st);
@@ -428,8 +430,13 @@ cudaError_t launch_error_stats(const QArgs& a, kvq_err* out_dev, cudaStream_t st
     const QSpec& q = a.q;
     const Geometry G = geometry(q, sm_count());
     Partial* partials = static_cast<Partial*>(a.ws);
-    const int64_t nblocks = (int64_t)G.grid.x * G.grid.y;
-    if (q.Tq == 0) {
+    int64_t nblocks = (int64_t)G.grid.x * G.grid.y;
+    const int64_t fast_blocks = fast_stats_blocks(q, sm_count());
+    if (q.Tq > 0 && fast_blocks > 0) {
+        nblocks = fast_blocks;
+        cudaError_t e = fast_error_stats(a, partials, st);
+        if (e != cudaSuccess) return e;
+    } else if (q.Tq == 0) {
         cudaError_t e = cudaMemsetAsync(partials, 0, (size_t)nblocks * sizeof(Partial), st);
         if (e != cudaSuccess) return e;
     } else if (q.x_dt == KVQ_BF16) {

@@ -48,6 +48,16 @@ cudaError_t launch_error_stats(const QArgs& a, kvq_err* out_dev, cudaStream_t st
 bool along_c_fast_ok(const QSpec& q);
 bool along_t_fast_ok(const QSpec& q);
 
+// ---- bf16 fast paths (fast.cu): used whenever they support the shape
+bool fast_quantize_supported(const QSpec& q);
+bool fast_quantize_copies_residual(const QSpec& q);
+size_t fast_quantize_workspace(const QSpec& q);
+cudaError_t fast_quantize(const QArgs& a, cudaStream_t st);
+bool fast_dequant_supported(const QSpec& q, int out_dt);
+cudaError_t fast_dequantize(const QArgs& a, cudaStream_t st);
+int64_t fast_stats_blocks(const QSpec& q, int sms);   // -1: not supported
+cudaError_t fast_error_stats(const QArgs& a, void* partials, cudaStream_t st);
+
 // ---- keep-set selection (select.cu) and compaction (compact.cu)
 struct SelectArgs {
     const float* hist;

@@ -525,6 +525,7 @@ cudaError_t dispatch_bits(const QArgs& a, cudaStream_t st)
 
 size_t quantize_workspace(const QSpec& q)
 {
+    if (fast_quantize_supported(q)) return fast_quantize_workspace(q);
     if (q.axis == KVQ_GROUP_ALONG_T && along_t_fast_ok(q) && q.g > kSliceRows && q.Tq > 0)
         return (size_t)(q.outer * q.ngroups * q.C) * 4 * (q.mode == KVQ_ASYM ? 2 : 1);
     return 0;
@@ -538,6 +539,13 @@ cudaError_t launch_quantize(const QArgs& a, cudaStream_t st)
         const int64_t n = q.outer * q.R * q.C;
         const int es = q.x_dt == KVQ_BF16 ? 2 : 4;
         copy_residual_kernel<<<(unsigned)grid_for(n, kThreads), kThreads, 0, st>>>(a, n, es);
+        return cudaGetLastError();
+    }
+    if (fast_quantize_supported(q)) {
+        cudaError_t e = fast_quantize(a, st);
+        if (e != cudaSuccess || fast_quantize_copies_residual(q) || q.R == 0) return e;
+        const int64_t n = q.outer * q.R * q.C;
+        copy_residual_kernel<<<(unsigned)grid_for(n, kThreads), kThreads, 0, st>>>(a, n, 2);
         return cudaGetLastError();
     }
     return q.x_dt == KVQ_BF16 ? dispatch_bits<__nv_bfloat16>(a, st) : dispatch_bits<float>(a, st);
