@@ -81,16 +81,17 @@ __device__ void block_reduce_store(const Acc& A, Partial* partials)
     }
 }
 
-// Final reduction over all block partials, fixed order.
-__global__ void __launch_bounds__(256) finalize_stats_kernel(const Partial* partials, int64_t n,
-                                                             double N, kvq_err* out)
+// Final reduction over all block partials, fixed order (1024 threads, so a
+// launch of up to a few thousand blocks needs one or two loads per thread).
+__global__ void __launch_bounds__(1024) finalize_stats_kernel(const Partial* partials, int64_t n,
+                                                              double N, kvq_err* out)
 {
-    __shared__ double s1[256], s2[256], mx[256];
+    __shared__ double s1[1024], s2[1024], mx[1024];
     double a = 0.0, b = 0.0, m = 0.0;
-    for (int64_t i = threadIdx.x; i < n; i += 256) { a += partials[i].s1; b += partials[i].s2; m = fmax(m, partials[i].mx); }
+    for (int64_t i = threadIdx.x; i < n; i += 1024) { a += partials[i].s1; b += partials[i].s2; m = fmax(m, partials[i].mx); }
     s1[threadIdx.x] = a; s2[threadIdx.x] = b; mx[threadIdx.x] = m;
     __syncthreads();
-    for (int o = 128; o > 0; o >>= 1) {
+    for (int o = 512; o > 0; o >>= 1) {
         if (threadIdx.x < o) {
             s1[threadIdx.x] += s1[threadIdx.x + o];
             s2[threadIdx.x] += s2[threadIdx.x + o];
@@ -444,7 +445,7 @@ cudaError_t launch_error_stats(const QArgs& a, kvq_err* out_dev, cudaStream_t st
     } else {
         launch_bits<float, true>(a, G, partials, st);
     }
-    finalize_stats_kernel<<<1, 256, 0, st>>>(partials, nblocks, (double)(q.outer * q.T * q.C), out_dev);
+    finalize_stats_kernel<<<1, 1024, 0, st>>>(partials, nblocks, (double)(q.outer * q.T * q.C), out_dev);
     return cudaGetLastError();
 }
 

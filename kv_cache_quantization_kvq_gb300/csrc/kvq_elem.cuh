@@ -1,0 +1,208 @@
+// kvq_elem.cuh -- element-level pieces shared by the bf16 fast kernels
+// (fast.cu, staged.cu): group constants, eight-element quantize / dequantize
+// steps, statistics accumulators and the per-block partial reduction.
+#pragma once
+
+#include "kvq_fast.cuh"
+
+namespace kvq {
+namespace elem {
+
+constexpr int kThr = 256;
+
+struct Partial { double s1, s2, mx; };
+
+// ---------------------------------------------------------------- group constants
+
+struct GroupC {
+    float s, inv, zp;   // scale and zero point as stored, RN(1/s)
+    int32_t zoff;       // clean code = bits(rint(q)+1.5*2^23) + zoff
+    bool fast;          // the fast quotient's preconditions hold
+};
+
+// off = 2^(bits-1) for signed codes (offset binary in registers), else 0
+template <bool ASYM>
+__device__ __forceinline__ GroupC make_group(float mn, float mx, const QSpec& q, int off) {
+    GroupC g;
+    Meta m;
+    float amag;
+    if (ASYM) {
+        m = meta_asym(mn, mx, q);
+        amag = fmaxf(fabsf(mn), fabsf(mx));
+    } else {
+        m = meta_sym(mx, q);      // mx carries the abs-max
+        amag = mx;
+    }
+    g.s = m.s;
+    g.zp = m.z;
+    g.inv = __frcp_rn(m.s);
+    g.fast = quot_ok(m.s, g.inv, amag) && fabsf(m.z) < 0x1p21f;
+    g.zoff = (ASYM ? (int32_t)m.z : 0) + off - (int32_t)kMagicBits;
+    return g;
+}
+
+// Eight elements (one uint4 of bf16) -> eight clean codes, fast quotient.
+// kq holds the four pairs' quotient constants; zo[j] the per-element offset.
+template <bool ASYM>
+__device__ __forceinline__ void codes8_fast(const uint4& w, const QuotK (&kq)[4], const int32_t (&zo)[8],
+                                            int lo_c, int hi_c, uint32_t (&c)[8]) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const u64 r = rint_bits2(quot2(widen_bf16x2(ws[j]), kq[j]));
+        if (ASYM) {
+            c[2 * j] = (uint32_t)min(__viaddmax_s32((int)lo_bits(r), zo[2 * j], lo_c), hi_c);
+            c[2 * j + 1] = (uint32_t)min(__viaddmax_s32((int)hi_bits(r), zo[2 * j + 1], lo_c), hi_c);
+        } else {
+            c[2 * j] = lo_bits(r) + (uint32_t)zo[2 * j];
+            c[2 * j + 1] = hi_bits(r) + (uint32_t)zo[2 * j + 1];
+        }
+    }
+}
+
+// Same codes through the IEEE division (groups outside the fast domain).
+template <bool ASYM>
+__device__ __forceinline__ void codes8_slow(const uint4& w, const float (&s)[8], const float (&zp)[8],
+                                            const QSpec& q, int off, uint32_t (&c)[8]) {
+    float v[8];
+    Raw8<__nv_bfloat16> raw;
+    raw.u = w;
+    widen8(raw, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        Meta m;
+        m.s = s[j];
+        m.z = zp[j];
+        c[j] = (uint32_t)(quant_code<ASYM>(v[j], m, q.lo, q.hi) + off);
+    }
+}
+
+template <int BITS>
+__device__ __forceinline__ typename CodeWord<BITS>::T finish_word(const uint32_t (&c)[8], bool is_signed) {
+    typename CodeWord<BITS>::T w = pack_clean8<BITS>(c);
+    return is_signed ? flip_signs<BITS>(w) : w;
+}
+
+template <int BITS>
+__device__ __forceinline__ void store_codes(uint8_t* p, typename CodeWord<BITS>::T w) {
+    *reinterpret_cast<typename CodeWord<BITS>::T*>(p) = w;
+}
+
+// bf16x2 min/max folding of 4 words
+__device__ __forceinline__ void fold_minmax(const uint4& w, uint32_t& mn, uint32_t& mx) {
+    mn = bmin2(bmin2(mn, w.x), bmin2(w.y, bmin2(w.z, w.w)));
+    mx = bmax2(bmax2(mx, w.x), bmax2(w.y, bmax2(w.z, w.w)));
+}
+__device__ __forceinline__ void fold_absmax(const uint4& w, uint32_t& mx) {
+    mx = bmax2(bmax2(mx, babs2(w.x)), bmax2(babs2(w.y), bmax2(babs2(w.z), babs2(w.w))));
+}
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+constexpr uint32_t kBfPosInf2 = 0x7F807F80u, kBfNegInf2 = 0xFF80FF80u;
+
+// Kahan-compensated float32 pair accumulators, one max as float bits.
+struct Acc2 {
+    float s1 = 0.0f, e1 = 0.0f, s2 = 0.0f, e2 = 0.0f;
+    uint32_t mxb = 0;
+    __device__ __forceinline__ static void kahan(float& s, float& e, float v) {
+        const float y = __fsub_rn(v, e);
+        const float t = __fadd_rn(s, y);
+        e = __fsub_rn(__fsub_rn(t, s), y);
+        s = t;
+    }
+    __device__ __forceinline__ void fold(u64 a1, u64 a2) {   // a tile's pair sums
+        kahan(s1, e1, __fadd_rn(lo_of(a1), hi_of(a1)));
+        kahan(s2, e2, __fadd_rn(lo_of(a2), hi_of(a2)));
+    }
+};
+
+// x_hat of eight codes (biased fields u) -> bf16x8; with STATS the
+// differences against the source word xw are accumulated instead.
+template <bool STATS>
+__device__ __forceinline__ uint4 dq8(const uint32_t (&u)[8], const u64 (&cp)[4], const u64 (&sp)[4],
+                                    const uint4& xw, u64& a1, u64& a2, uint32_t& mxb) {
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const u64 v = mul2(sub2(pk(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1])), cp[j]), sp[j]);
+        o[j] = pack_bf16x2(lo_of(v), hi_of(v));
+    }
+    if (STATS) {
+        const uint32_t xs[4] = {xw.x, xw.y, xw.z, xw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const u64 d = sub2(widen_bf16x2(xs[j]), widen_bf16x2(o[j]));
+            const uint32_t al = lo_bits(d) & 0x7FFFFFFFu, ah = hi_bits(d) & 0x7FFFFFFFu;
+            a1 = add2(a1, pk(__uint_as_float(al), __uint_as_float(ah)));
+            a2 = fma2(d, d, a2);
+            mxb = (uint32_t)__vimax3_s32((int)mxb, (int)al, (int)ah);
+        }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// exact slow path for groups whose zero point is too large for the biased
+// form: q = field - off, then ((float)q - zp) * s exactly as the reference
+template <bool STATS>
+__device__ __forceinline__ uint4 dq8_slow(const uint32_t (&u)[8], int off, const float (&zp)[8], const float (&s)[8],
+                                         const uint4& xw, u64& a1, u64& a2, uint32_t& mxb) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        Meta m;
+        m.s = s[j];
+        m.z = zp[j];
+        v[j] = dequant_value((int)(u[j] - kTwo23Bits) - off, m);
+    }
+    uint4 out;
+    out.x = pack_bf16x2(v[0], v[1]);
+    out.y = pack_bf16x2(v[2], v[3]);
+    out.z = pack_bf16x2(v[4], v[5]);
+    out.w = pack_bf16x2(v[6], v[7]);
+    if (STATS) {
+        const uint32_t xs[4] = {xw.x, xw.y, xw.z, xw.w}, os[4] = {out.x, out.y, out.z, out.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const u64 d = sub2(widen_bf16x2(xs[j]), widen_bf16x2(os[j]));
+            const uint32_t al = lo_bits(d) & 0x7FFFFFFFu, ah = hi_bits(d) & 0x7FFFFFFFu;
+            a1 = add2(a1, pk(__uint_as_float(al), __uint_as_float(ah)));
+            a2 = fma2(d, d, a2);
+            mxb = (uint32_t)__vimax3_s32((int)mxb, (int)al, (int)ah);
+        }
+    }
+    return out;
+}
+
+__device__ __forceinline__ void block_reduce_partial(const Acc2& A, Partial* partials)
+{
+    __shared__ double sh1[kThr / 32], sh2[kThr / 32], shm[kThr / 32];
+    double s1 = (double)A.s1 - (double)A.e1;
+    double s2 = (double)A.s2 - (double)A.e2;
+    double mx = (double)__uint_as_float(A.mxb);
+    for (int o = 16; o > 0; o >>= 1) {
+        s1 += __shfl_xor_sync(0xFFFFFFFFu, s1, o);
+        s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, o);
+        mx = fmax(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) { sh1[w] = s1; sh2[w] = s2; shm[w] = mx; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Partial p = {0.0, 0.0, 0.0};
+        for (int i = 0; i < kThr / 32; ++i) { p.s1 += sh1[i]; p.s2 += sh2[i]; p.mx = fmax(p.mx, shm[i]); }
+        partials[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = p;
+    }
+}
+
+// Per-group dequant constants: biased subtrahend 2^23 + off + zp and the scale.
+__device__ __forceinline__ void dq_consts(float s, float zp, int off, u64& cp_half, u64& sp_half, bool& fast) {
+    fast = fabsf(zp) < 0x1p21f;
+    const float c = __fadd_rn(8388608.0f + (float)off, zp);     // exact when |zp| < 2^21
+    cp_half = pk(c, c);
+    sp_half = pk(s, s);
+}
+
+
+}  // namespace elem
+}  // namespace kvq

@@ -58,6 +58,14 @@ cudaError_t fast_dequantize(const QArgs& a, cudaStream_t st);
 int64_t fast_stats_blocks(const QSpec& q, int sms);   // -1: not supported
 cudaError_t fast_error_stats(const QArgs& a, void* partials, cudaStream_t st);
 
+// ---- staged quantize and streaming dequantize / statistics (staged.cu)
+bool staged_quantize_supported(const QSpec& q);
+bool staged_quantize(const QArgs& a, cudaStream_t st);          // false: not handled
+bool stream_dequant_supported(const QSpec& q, int out_dt);
+cudaError_t stream_dequantize(const QArgs& a, cudaStream_t st);
+int64_t stream_stats_blocks(const QSpec& q, int sms);           // -1: not supported
+cudaError_t stream_error_stats(const QArgs& a, void* partials, cudaStream_t st);
+
 // ---- keep-set selection (select.cu) and compaction (compact.cu)
 struct SelectArgs {
     const float* hist;

@@ -1,0 +1,671 @@
+// staged.cu -- quantize kernels fed by bulk asynchronous copies, and the
+// coalesced streaming dequantize / statistics kernel (bf16 sources).
+//
+// Method: "KV Compression 公式到源码对照" §1.1-§1.3 and "KV cache 压缩：
+// 把历史装得更小" (group-wise form, KIVI axes, residual window); same results
+// as the other kernels, bit for bit.
+//
+// Quantize.  A persistent CTA walks 16 KB chunks of the source that are
+// contiguous in memory: one group tile [g tokens x C channels] for groups
+// along T (K), or 8192/C whole token rows for groups along C (V).  One thread
+// issues cp.async.bulk into a 4-stage shared-memory ring, completion is
+// signalled on an mbarrier per stage, so each SM keeps several chunks in
+// flight without registers holding them.  Threads then read the chunk from
+// shared memory, reduce each group, derive its constants once, and write
+// codes and metadata with coalesced stores.
+//
+// Dequantize / statistics.  Lane = 8 channels of RPT consecutive tokens;
+// lanes of a warp cover consecutive channel chunks, so every code load,
+// source load and output store is coalesced; group constants are loaded once
+// per lane item.
+#include <algorithm>
+
+#include "kvq_bulk.cuh"
+#include "kvq_elem.cuh"
+
+namespace kvq {
+
+namespace {
+
+using namespace elem;
+
+constexpr int kStages = 4;
+constexpr int kStageBytes = 16384;
+constexpr int kStagedSmem = kStages * kStageBytes + 64;   // ring + barriers
+
+struct ChunkSrc { const void* ptr; uint32_t bytes; };
+
+// metadata element of a compile-time dtype, widened to float
+template <int DT>
+__device__ __forceinline__ float ld_meta(const void* p, int64_t i) {
+    if constexpr (DT == KVQ_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+    else if constexpr (DT == KVQ_I8) return (float)static_cast<const int8_t*>(p)[i];
+    else return static_cast<const float*>(p)[i];
+}
+template <int DT>
+__device__ __forceinline__ void st_meta(void* p, int64_t i, float v) {
+    if constexpr (DT == KVQ_BF16) static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+    else if constexpr (DT == KVQ_I8) static_cast<int8_t*>(p)[i] = (int8_t)(int)v;
+    else if constexpr (DT == KVQ_F32) static_cast<float*>(p)[i] = v;
+}
+template <int SDT, int ZDT>
+__device__ __forceinline__ void write_meta_t(const QArgs& a, int64_t i, const GroupC& g) {
+    st_meta<SDT>(a.scale, i, g.s);
+    if constexpr (ZDT != KVQ_NONE) st_meta<ZDT>(a.zero, i, g.zp);
+}
+
+// The persistent chunk loop.  src(c) gives chunk c's source bytes, body(c,
+// smem) consumes it; body is called by every thread of the CTA.
+template <typename SrcFn, typename BodyFn>
+__device__ __forceinline__ void staged_loop(uint64_t nchunks, SrcFn src, BodyFn body)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const uint64_t first = blockIdx.x, step = gridDim.x;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            const uint64_t c = first + (uint64_t)s * step;
+            if (c < nchunks) {
+                const ChunkSrc cs = src(c);
+                mbar_expect_tx(&bars[s], cs.bytes);
+                bulk_g2s(smem + s * kStageBytes, cs.ptr, cs.bytes, &bars[s]);
+            }
+        }
+    }
+    for (uint64_t k = 0;; ++k) {
+        const uint64_t c = first + k * step;
+        if (c >= nchunks) break;
+        const int s = (int)(k % kStages);
+        const uint32_t parity = (uint32_t)((k / kStages) & 1u);
+        const bool ok = __syncthreads_and(mbar_wait(&bars[s], parity));
+        if (!ok) return;                           // recorded in g_kvq_wait_timeouts
+        body(c, smem + s * kStageBytes);
+        __syncthreads();                           // the stage is free again
+        if (threadIdx.x == 0) {
+            const uint64_t n = c + (uint64_t)kStages * step;
+            if (n < nchunks) {
+                const ChunkSrc cs = src(n);
+                mbar_expect_tx(&bars[s], cs.bytes);
+                bulk_g2s(smem + s * kStageBytes, cs.ptr, cs.bytes, &bars[s]);
+            }
+        }
+    }
+}
+
+// ======================================================================
+// groups along T: chunk = group tile [G tokens x C channels], C in {64,128,256}
+// ======================================================================
+template <int BITS, bool ASYM, int C, int SDT, int ZDT>
+__global__ void __launch_bounds__(kThr)
+sq_t_kernel(const QArgs a)
+{
+    constexpr int L8 = C / 8;                 // threads across a row (8 channels each)
+    constexpr int NR = kThr / L8;             // row slices
+    constexpr int MAXG = kStageBytes / (2 * C);
+    constexpr int RPTH = (MAXG + NR - 1) / NR; // rows per thread at most
+    constexpr int NW = kThr / 32;
+    __shared__ uint32_t red_mn[NW][L8][4], red_mx[NW][L8][4];
+    __shared__ __align__(16) float c_s[C], c_i[C];
+    __shared__ __align__(16) int32_t c_z[C];
+
+    const QSpec& q = a.q;
+    const int t = threadIdx.x, c8 = t % L8, rs = t / L8, warp = t >> 5, lane = t & 31;
+    const int off = q.is_signed ? (1 << (BITS - 1)) : 0;
+    const int lo_c = q.qmin + off, hi_c = q.qmax + off;
+    const int G = (int)q.g;
+    const uint32_t ng = (uint32_t)q.ngroups;
+    const uint32_t nres = (uint32_t)((q.R + G - 1) / G);
+    const uint32_t per_o = ng + nres;
+    const uint64_t nchunks = (uint64_t)q.outer * per_o;
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+    uint8_t* codes = static_cast<uint8_t*>(a.codes);
+    const uint64_t code_row_B = (uint64_t)C * BITS / 8;
+
+    const uint32_t Tq32 = (uint32_t)q.Tq, T32 = (uint32_t)q.T;
+    // chunk -> (outer, group or residual slot k, first row, rows); 32-bit math
+    auto geom = [&](uint64_t c, uint32_t& o, uint32_t& k, uint32_t& row0, int& nrows, bool& res) {
+        const uint32_t c32 = (uint32_t)c;
+        o = c32 / per_o;
+        k = c32 - o * per_o;
+        res = k >= ng;
+        row0 = res ? Tq32 + (k - ng) * (uint32_t)G : k * (uint32_t)G;
+        const uint32_t end = res ? T32 : Tq32;
+        nrows = (int)min((uint32_t)G, end - row0);
+    };
+    auto src = [&](uint64_t c) {
+        uint32_t o, k, row0; int nrows; bool res;
+        geom(c, o, k, row0, nrows, res);
+        return ChunkSrc{x + ((uint64_t)o * T32 + row0) * C, (uint32_t)(nrows * C * 2)};
+    };
+    auto body = [&](uint64_t c, const unsigned char* buf) {
+        uint32_t o, k, row0; int nrows; bool res;
+        geom(c, o, k, row0, nrows, res);
+        uint4 w[RPTH];
+#pragma unroll
+        for (int j = 0; j < RPTH; ++j) {
+            const int r = rs + NR * j;
+            w[j] = r < nrows ? *reinterpret_cast<const uint4*>(buf + (size_t)r * C * 2 + c8 * 16) : make_uint4(0, 0, 0, 0);
+        }
+        if (res) {
+            __nv_bfloat16* resid = static_cast<__nv_bfloat16*>(a.resid);
+#pragma unroll
+            for (int j = 0; j < RPTH; ++j) {
+                const int r = rs + NR * j;
+                if (r < nrows)
+                    *reinterpret_cast<uint4*>(resid + (((uint64_t)o * q.R + (row0 - Tq32) + r) * C + c8 * 8)) = w[j];
+            }
+            return;
+        }
+        // per-thread statistics over its rows, then over the warp's row slices
+        uint32_t mn[4], mx[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) { mn[p] = kBfPosInf2; mx[p] = ASYM ? kBfNegInf2 : 0u; }
+#pragma unroll
+        for (int j = 0; j < RPTH; ++j) {
+            if (rs + NR * j < nrows) {
+                const uint32_t ws[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    if (ASYM) { mn[p] = bmin2(mn[p], ws[p]); mx[p] = bmax2(mx[p], ws[p]); }
+                    else mx[p] = bmax2(mx[p], babs2(ws[p]));
+                }
+            }
+        }
+#pragma unroll
+        for (int sft = L8; sft < 32; sft <<= 1) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                if (ASYM) mn[p] = bmin2(mn[p], __shfl_xor_sync(0xFFFFFFFFu, mn[p], sft));
+                mx[p] = bmax2(mx[p], __shfl_xor_sync(0xFFFFFFFFu, mx[p], sft));
+            }
+        }
+        if (L8 >= 32 || lane < L8) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                red_mn[warp][c8][p] = mn[p];
+                red_mx[warp][c8][p] = mx[p];
+            }
+        }
+        __syncthreads();
+        // one thread per channel: constants and metadata
+        bool fast = true;
+        if (t < C) {
+            const int cc8 = t / 8, p = (t % 8) / 2, half = t & 1;
+            constexpr int WARPS_WITH_DATA = L8 >= 32 ? NW : NW;   // every warp holds a partial
+            uint32_t wm = red_mn[0][cc8][p], wx = red_mx[0][cc8][p];
+#pragma unroll
+            for (int wi = 1; wi < WARPS_WITH_DATA; ++wi) {
+                if (ASYM) wm = bmin2(wm, red_mn[wi][cc8][p]);
+                wx = bmax2(wx, red_mx[wi][cc8][p]);
+            }
+            const float fmn = half ? hi_f(wm) : lo_f(wm);
+            const float fmx = half ? hi_f(wx) : lo_f(wx);
+            const GroupC gc = make_group<ASYM>(fmn, fmx, q, off);
+            write_meta_t<SDT, ZDT>(a, ((int64_t)o * ng + k) * C + t, gc);
+            c_s[t] = gc.s;
+            c_i[t] = gc.inv;
+            c_z[t] = gc.zoff;
+            fast = gc.fast;
+        }
+        const bool all_fast = __syncthreads_and(fast);
+        float s8[8], i8[8], z8f[8];
+        int32_t zo[8];
+        {
+            const float4* ps = reinterpret_cast<const float4*>(c_s + c8 * 8);
+            const float4* pi = reinterpret_cast<const float4*>(c_i + c8 * 8);
+            const int4* pz = reinterpret_cast<const int4*>(c_z + c8 * 8);
+            const float4 s0 = ps[0], s1 = ps[1], i0 = pi[0], i1 = pi[1];
+            const int4 z0 = pz[0], z1 = pz[1];
+            s8[0] = s0.x; s8[1] = s0.y; s8[2] = s0.z; s8[3] = s0.w; s8[4] = s1.x; s8[5] = s1.y; s8[6] = s1.z; s8[7] = s1.w;
+            i8[0] = i0.x; i8[1] = i0.y; i8[2] = i0.z; i8[3] = i0.w; i8[4] = i1.x; i8[5] = i1.y; i8[6] = i1.z; i8[7] = i1.w;
+            zo[0] = z0.x; zo[1] = z0.y; zo[2] = z0.z; zo[3] = z0.w; zo[4] = z1.x; zo[5] = z1.y; zo[6] = z1.z; zo[7] = z1.w;
+        }
+        uint8_t* cbase = codes + ((uint64_t)o * q.Tq + row0) * code_row_B + (uint64_t)c8 * BITS;
+        if (all_fast) {
+            QuotK kq[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                kq[p].ns = pk(-s8[2 * p], -s8[2 * p + 1]);
+                kq[p].inv = pk(i8[2 * p], i8[2 * p + 1]);
+            }
+#pragma unroll
+            for (int j = 0; j < RPTH; ++j) {
+                const int r = rs + NR * j;
+                if (r < nrows) {
+                    uint32_t cc[8];
+                    codes8_fast<ASYM>(w[j], kq, zo, lo_c, hi_c, cc);
+                    store_codes<BITS>(cbase + (uint64_t)r * code_row_B, finish_word<BITS>(cc, q.is_signed));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) z8f[j] = (float)(zo[j] - off + (int32_t)kMagicBits);
+#pragma unroll
+            for (int j = 0; j < RPTH; ++j) {
+                const int r = rs + NR * j;
+                if (r < nrows) {
+                    uint32_t cc[8];
+                    codes8_slow<ASYM>(w[j], s8, z8f, q, off, cc);
+                    store_codes<BITS>(cbase + (uint64_t)r * code_row_B, finish_word<BITS>(cc, q.is_signed));
+                }
+            }
+        }
+    };
+    staged_loop(nchunks, src, body);
+}
+
+// ======================================================================
+// groups along C: chunk = 8192/C whole token rows; thread = 32 channels
+// ======================================================================
+template <int BITS, bool ASYM, int G, int SDT, int ZDT>
+__global__ void __launch_bounds__(kThr)
+sq_c_kernel(const QArgs a)
+{
+    constexpr int GPT = G >= 32 ? 1 : 32 / G;    // groups per thread
+    constexpr int TPG = G >= 32 ? G / 32 : 1;    // threads per group
+    constexpr int WPG = G >= 32 ? 4 : G / 8;     // 8-element words per group in a thread
+    const QSpec& q = a.q;
+    const int t = threadIdx.x;
+    const int C = (int)q.C;
+    const int TPR = C / 32;                      // threads per row
+    const int RC = kStageBytes / (2 * C);        // rows per chunk
+    const int r = t / TPR, part = t - r * TPR;
+    const int off = q.is_signed ? (1 << (BITS - 1)) : 0;
+    const int lo_c = q.qmin + off, hi_c = q.qmax + off;
+    const uint32_t T = (uint32_t)q.T, Tq = (uint32_t)q.Tq;
+    const uint64_t nrows_total = (uint64_t)q.outer * q.T;
+    const uint64_t nchunks = (nrows_total + RC - 1) / RC;
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+    uint8_t* codes = static_cast<uint8_t*>(a.codes);
+    const int gpr = C / G;
+
+    auto src = [&](uint64_t c) {
+        const uint64_t row0 = c * RC;
+        const uint64_t n = min((uint64_t)RC, nrows_total - row0);
+        return ChunkSrc{x + row0 * C, (uint32_t)(n * C * 2)};
+    };
+    auto body = [&](uint64_t c, const unsigned char* buf) {
+        const uint64_t grow = c * RC + r;
+        const bool valid = r < RC && grow < nrows_total;
+        uint4 w[4];
+        const unsigned char* p = buf + (size_t)r * C * 2 + part * 64;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[k] = valid ? *reinterpret_cast<const uint4*>(p + k * 16) : make_uint4(0, 0, 0, 0);
+        const uint32_t g32 = (uint32_t)grow;
+        const uint32_t o = valid ? g32 / T : 0u;
+        const uint32_t tt = valid ? g32 - o * T : 0u;
+        // group statistics
+        float gmn[GPT], gmx[GPT];
+#pragma unroll
+        for (int gg = 0; gg < GPT; ++gg) {
+            uint32_t mn = kBfPosInf2, mx = ASYM ? kBfNegInf2 : 0u;
+#pragma unroll
+            for (int k = 0; k < WPG; ++k) {
+                if (ASYM) fold_minmax(w[gg * WPG + k], mn, mx);
+                else fold_absmax(w[gg * WPG + k], mx);
+            }
+            gmn[gg] = fminf(lo_f(mn), hi_f(mn));
+            gmx[gg] = fmaxf(lo_f(mx), hi_f(mx));
+#pragma unroll
+            for (int sft = 1; sft < TPG; sft <<= 1) {
+                gmn[gg] = fminf(gmn[gg], __shfl_xor_sync(0xFFFFFFFFu, gmn[gg], sft));
+                gmx[gg] = fmaxf(gmx[gg], __shfl_xor_sync(0xFFFFFFFFu, gmx[gg], sft));
+            }
+        }
+        if (!valid) return;
+        if (tt >= Tq) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.resid) +
+                                                 (((uint64_t)o * q.R + (tt - Tq)) * C + (uint64_t)part * 32));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = w[k];
+            return;
+        }
+        const uint64_t qrow = (uint64_t)o * Tq + tt;
+        typename CodeWord<BITS>::T cw[4];
+#pragma unroll
+        for (int gg = 0; gg < GPT; ++gg) {
+            const GroupC gc = make_group<ASYM>(gmn[gg], gmx[gg], q, off);
+            const int64_t gidx = G >= 32 ? (int64_t)part / TPG : (int64_t)part * GPT + gg;
+            if (TPG == 1 || (part % TPG) == 0) write_meta_t<SDT, ZDT>(a, (int64_t)qrow * gpr + gidx, gc);
+            if (gc.fast) {
+                QuotK kq[4];
+                kq[0].ns = pk(-gc.s, -gc.s);
+                kq[0].inv = pk(gc.inv, gc.inv);
+                kq[1] = kq[2] = kq[3] = kq[0];
+                int32_t zo[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) zo[j] = gc.zoff;
+#pragma unroll
+                for (int k = 0; k < WPG; ++k) {
+                    uint32_t cc[8];
+                    codes8_fast<ASYM>(w[gg * WPG + k], kq, zo, lo_c, hi_c, cc);
+                    cw[gg * WPG + k] = finish_word<BITS>(cc, q.is_signed);
+                }
+            } else {
+                float s8[8], z8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) { s8[j] = gc.s; z8[j] = gc.zp; }
+#pragma unroll
+                for (int k = 0; k < WPG; ++k) {
+                    uint32_t cc[8];
+                    codes8_slow<ASYM>(w[gg * WPG + k], s8, z8, q, off, cc);
+                    cw[gg * WPG + k] = finish_word<BITS>(cc, q.is_signed);
+                }
+            }
+        }
+        uint8_t* cdst = codes + qrow * (uint64_t)(C * BITS / 8) + (uint64_t)part * 4 * BITS;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) store_codes<BITS>(cdst + k * BITS, cw[k]);
+    };
+    staged_loop(nchunks, src, body);
+}
+
+// ======================================================================
+// dequantize / statistics: lane = 8 channels x RPT tokens
+// ======================================================================
+// Constants of one group for all four pairs of a lane's eight channels.
+__device__ __forceinline__ void dq_pair_consts(float s, float z, int off, u64& cp, u64& sp) {
+    const float c = __fadd_rn(8388608.0f + (float)off, z);
+    cp = pk(c, c);
+    sp = pk(s, s);
+}
+
+template <int BITS, bool ASYM, bool ALONG_T, int RPT, bool STATS, int SDT, int ZDT>
+__global__ void __launch_bounds__(kThr)
+ds_kernel(const QArgs a, int lcpr, int lg, Partial* partials)
+{
+    const QSpec& q = a.q;
+    const int off = q.is_signed ? (1 << (BITS - 1)) : 0;
+    const int64_t C = q.C;
+    const uint32_t cpr = 1u << lcpr;                         // 8-channel chunks per row
+    const int64_t Tq = q.Tq;
+    const uint32_t nrb_q = (uint32_t)(Tq / RPT);              // full row blocks of quantized tokens
+    const uint32_t nrb = (uint32_t)((q.T + RPT - 1) / RPT);  // all row blocks
+    const uint64_t items_per_o = (uint64_t)nrb << lcpr;
+    const uint8_t* codes = static_cast<const uint8_t*>(a.codes);
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    const __nv_bfloat16* resid = static_cast<const __nv_bfloat16*>(a.resid);
+    const uint64_t code_row_B = (uint64_t)C * BITS / 8;
+    const uint32_t gpr = ALONG_T ? 0u : (uint32_t)q.ngroups;  // groups per row (along C)
+    using W = typename CodeWord<BITS>::T;
+    Acc2 A;
+    for (uint64_t o = blockIdx.y; o < (uint64_t)q.outer; o += gridDim.y) {
+        for (uint64_t it = (uint64_t)blockIdx.x * kThr + threadIdx.x; it < items_per_o;
+             it += (uint64_t)gridDim.x * kThr) {
+            const uint32_t c8 = (uint32_t)(it & (cpr - 1));
+            const uint32_t rb = (uint32_t)(it >> lcpr);
+            const int64_t t0 = (int64_t)rb * RPT;
+            const uint64_t cofs = (uint64_t)c8 * 8;
+            if (rb < nrb_q) {
+                // RPT quantized rows
+                const W* cptr = reinterpret_cast<const W*>(codes + ((uint64_t)o * Tq + t0) * code_row_B) + c8;
+                const size_t cstride = code_row_B / sizeof(W);
+                const uint4* xptr = reinterpret_cast<const uint4*>(x + ((o * (uint64_t)q.T + t0) * C + cofs));
+                uint4* optr = reinterpret_cast<uint4*>(out + ((o * (uint64_t)q.T + t0) * C + cofs));
+                const size_t vstride = (size_t)C / 8;
+                W cw[RPT];
+                uint4 xw[RPT];
+#pragma unroll
+                for (int j = 0; j < RPT; ++j) {
+                    cw[j] = __ldcs(cptr + j * cstride);
+                    if (STATS) xw[j] = __ldcs(xptr + j * vstride);
+                }
+                u64 cp[4], sp[4];
+                bool fast_t = true;
+                if (ALONG_T) {
+                    // eight per-channel groups shared by the RPT rows
+                    const int64_t mi = ((int64_t)o * q.ngroups + (t0 >> lg)) * C + (int64_t)cofs;
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        const float s0 = ld_meta<SDT>(a.scale, mi + 2 * p);
+                        const float s1 = ld_meta<SDT>(a.scale, mi + 2 * p + 1);
+                        const float z0 = ASYM ? ld_meta<ZDT>(a.zero, mi + 2 * p) : 0.0f;
+                        const float z1 = ASYM ? ld_meta<ZDT>(a.zero, mi + 2 * p + 1) : 0.0f;
+                        cp[p] = pk(__fadd_rn(8388608.0f + (float)off, z0), __fadd_rn(8388608.0f + (float)off, z1));
+                        sp[p] = pk(s0, s1);
+                        fast_t = fast_t && fabsf(z0) < 0x1p21f && fabsf(z1) < 0x1p21f;
+                    }
+                }
+                u64 a1 = 0, a2 = 0;
+#pragma unroll
+                for (int j = 0; j < RPT; ++j) {
+                    float zs = 0.0f, ss = 1.0f;
+                    if (!ALONG_T) {
+                        const int64_t mi = ((int64_t)o * Tq + t0 + j) * gpr + (int64_t)(cofs >> lg);
+                        ss = ld_meta<SDT>(a.scale, mi);
+                        zs = ASYM ? ld_meta<ZDT>(a.zero, mi) : 0.0f;
+                        u64 c1, s1;
+                        dq_pair_consts(ss, zs, off, c1, s1);
+                        cp[0] = cp[1] = cp[2] = cp[3] = c1;
+                        sp[0] = sp[1] = sp[2] = sp[3] = s1;
+                    }
+                    uint32_t u[8];
+                    unpack_biased8<BITS>(q.is_signed ? flip_signs<BITS>(cw[j]) : cw[j], u);
+                    const bool fast = ALONG_T ? fast_t : (!ASYM || fabsf(zs) < 0x1p21f);
+                    uint4 ow;
+                    if (fast) {
+                        ow = dq8<STATS>(u, cp, sp, xw[j], a1, a2, A.mxb);
+                    } else {
+                        // exact reference order for groups with a very large zero point
+                        float sf[8], zf[8];
+                        const int64_t mi = ALONG_T ? ((int64_t)o * q.ngroups + (t0 >> lg)) * C + (int64_t)cofs
+                                                   : ((int64_t)o * Tq + t0 + j) * gpr + (int64_t)(cofs >> lg);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            sf[k] = ld_meta<SDT>(a.scale, ALONG_T ? mi + k : mi);
+                            zf[k] = ASYM ? ld_meta<ZDT>(a.zero, ALONG_T ? mi + k : mi) : 0.0f;
+                        }
+                        ow = dq8_slow<STATS>(u, off, zf, sf, xw[j], a1, a2, A.mxb);
+                    }
+                    if (!STATS) optr[j * vstride] = ow;
+                }
+                if (STATS) A.fold(a1, a2);
+            } else {
+                // tail: the last partial row block and the residual window
+                for (int j = 0; j < RPT; ++j) {
+                    const int64_t tr = t0 + j;
+                    if (tr >= q.T) break;
+                    const uint64_t xo = (o * (uint64_t)q.T + tr) * C + cofs;
+                    if (tr >= Tq) {
+                        if (!STATS)
+                            *reinterpret_cast<uint4*>(out + xo) =
+                                __ldcs(reinterpret_cast<const uint4*>(resid + ((o * (uint64_t)q.R + (tr - Tq)) * C + cofs)));
+                        continue;
+                    }
+                    const W w = __ldcs(reinterpret_cast<const W*>(codes + ((uint64_t)o * Tq + tr) * code_row_B + (uint64_t)c8 * BITS));
+                    const uint4 xv = STATS ? __ldcs(reinterpret_cast<const uint4*>(x + xo)) : make_uint4(0, 0, 0, 0);
+                    float sf[8], zf[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int64_t mi = ALONG_T ? ((int64_t)o * q.ngroups + (tr >> lg)) * C + (int64_t)cofs + k
+                                                   : ((int64_t)o * Tq + tr) * gpr + (int64_t)(cofs >> lg);
+                        sf[k] = ld_meta<SDT>(a.scale, mi);
+                        zf[k] = ASYM ? ld_meta<ZDT>(a.zero, mi) : 0.0f;
+                    }
+                    uint32_t u[8];
+                    unpack_biased8<BITS>(q.is_signed ? flip_signs<BITS>(w) : w, u);
+                    u64 a1 = 0, a2 = 0;
+                    const uint4 ow = dq8_slow<STATS>(u, off, zf, sf, xv, a1, a2, A.mxb);
+                    if (STATS) A.fold(a1, a2);
+                    else *reinterpret_cast<uint4*>(out + xo) = ow;
+                }
+            }
+        }
+    }
+    if (STATS) block_reduce_partial(A, partials);
+}
+
+int log2_exact(int64_t v) {
+    int l = 0;
+    while ((int64_t(1) << l) < v) ++l;
+    return (int64_t(1) << l) == v ? l : -1;
+}
+
+// Metadata layouts with dedicated kernels: 0 = bf16 scale + bf16 zero,
+// 1 = f32 scale + int8 zero (asymmetric); 2 = bf16 scale, 3 = f32 scale
+// (symmetric).  -1: handled by the other paths.
+int meta_kind(const QSpec& q) {
+    if (q.mode == KVQ_ASYM) {
+        if (q.scale_dt == KVQ_BF16 && q.zero_dt == KVQ_BF16) return 0;
+        if (q.scale_dt == KVQ_F32 && q.zero_dt == KVQ_I8) return 1;
+        return -1;
+    }
+    return q.scale_dt == KVQ_BF16 ? 2 : 3;
+}
+
+template <typename K>
+void ensure_smem(K kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedSmem);
+}
+
+unsigned staged_grid(int sms, uint64_t nchunks) {
+    // three CTAs of 64 KB ring per SM
+    return (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(nchunks, (uint64_t)sms * 3));
+}
+
+bool staged_t_ok(const QSpec& q) {
+    return q.x_dt == KVQ_BF16 && q.aligned && q.C == 128 && q.g * q.C * 2 <= kStageBytes && q.Tq > 0 &&
+           meta_kind(q) >= 0 && q.outer * (q.ngroups + (q.R + q.g - 1) / q.g) < (int64_t(1) << 31);
+}
+bool staged_c_ok(const QSpec& q) {
+    if (q.x_dt != KVQ_BF16 || !q.aligned || q.C % 32 != 0 || q.C > kStageBytes / 2) return false;
+    if ((kStageBytes / 2) % q.C != 0 || meta_kind(q) < 0) return false;      // whole rows per chunk
+    if (q.outer * q.T >= (int64_t(1) << 31)) return false;
+    const int64_t g = q.g;
+    return q.C % g == 0 && (g == 32 || g == 64 || g == 128);
+}
+
+template <int BITS, bool ASYM, int SDT, int ZDT>
+void sq_t_launch(const QArgs& a, cudaStream_t st) {
+    const QSpec& q = a.q;
+    const uint64_t nchunks = (uint64_t)q.outer * (q.ngroups + (q.R + q.g - 1) / q.g);
+    const unsigned grid = staged_grid(sm_count(), nchunks);
+    ensure_smem(sq_t_kernel<BITS, ASYM, 128, SDT, ZDT>);
+    sq_t_kernel<BITS, ASYM, 128, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a);
+}
+
+template <int BITS, bool ASYM, int SDT, int ZDT>
+void sq_c_launch(const QArgs& a, cudaStream_t st) {
+    const QSpec& q = a.q;
+    const uint64_t rc = kStageBytes / (2 * q.C);
+    const uint64_t nchunks = ((uint64_t)q.outer * q.T + rc - 1) / rc;
+    const unsigned grid = staged_grid(sm_count(), nchunks);
+    switch (q.g) {
+    case 32: ensure_smem(sq_c_kernel<BITS, ASYM, 32, SDT, ZDT>); sq_c_kernel<BITS, ASYM, 32, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a); break;
+    case 64: ensure_smem(sq_c_kernel<BITS, ASYM, 64, SDT, ZDT>); sq_c_kernel<BITS, ASYM, 64, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a); break;
+    default: ensure_smem(sq_c_kernel<BITS, ASYM, 128, SDT, ZDT>); sq_c_kernel<BITS, ASYM, 128, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a); break;
+    }
+}
+
+// (bits, meta kind) -> a launcher templated on the mode and metadata dtypes
+template <template <int, bool, int, int> class L>
+void by_meta(const QArgs& a, cudaStream_t st) {
+    const int mk = meta_kind(a.q);
+    switch (a.q.bits) {
+    case 8:
+        if (mk == 0) L<8, true, KVQ_BF16, KVQ_BF16>::run(a, st);
+        else if (mk == 1) L<8, true, KVQ_F32, KVQ_I8>::run(a, st);
+        else if (mk == 2) L<8, false, KVQ_BF16, KVQ_NONE>::run(a, st);
+        else L<8, false, KVQ_F32, KVQ_NONE>::run(a, st);
+        break;
+    case 4:
+        if (mk == 0) L<4, true, KVQ_BF16, KVQ_BF16>::run(a, st);
+        else if (mk == 1) L<4, true, KVQ_F32, KVQ_I8>::run(a, st);
+        else if (mk == 2) L<4, false, KVQ_BF16, KVQ_NONE>::run(a, st);
+        else L<4, false, KVQ_F32, KVQ_NONE>::run(a, st);
+        break;
+    default:
+        if (mk == 0) L<2, true, KVQ_BF16, KVQ_BF16>::run(a, st);
+        else if (mk == 1) L<2, true, KVQ_F32, KVQ_I8>::run(a, st);
+        else if (mk == 2) L<2, false, KVQ_BF16, KVQ_NONE>::run(a, st);
+        else L<2, false, KVQ_F32, KVQ_NONE>::run(a, st);
+        break;
+    }
+}
+
+template <int B, bool A, int S, int Z> struct SqT { static void run(const QArgs& a, cudaStream_t st) { sq_t_launch<B, A, S, Z>(a, st); } };
+template <int B, bool A, int S, int Z> struct SqC { static void run(const QArgs& a, cudaStream_t st) { sq_c_launch<B, A, S, Z>(a, st); } };
+
+// ---- dequantize / statistics geometry
+constexpr int kRpt = 4;
+
+bool ds_ok(const QSpec& q) {
+    if (q.x_dt != KVQ_BF16 || !q.aligned || q.C % 8 != 0 || log2_exact(q.C / 8) < 0 || meta_kind(q) < 0) return false;
+    if (log2_exact(q.g) < 0) return false;
+    if (q.axis == KVQ_GROUP_ALONG_T) return q.g % kRpt == 0;
+    return q.g % 8 == 0 && q.C % q.g == 0;
+}
+
+dim3 ds_grid(const QSpec& q, int sms) {
+    const int lcpr = log2_exact(q.C / 8);
+    const uint64_t items = (uint64_t)((q.T + kRpt - 1) / kRpt) << lcpr;
+    const unsigned gy = (unsigned)std::max<int64_t>(1, std::min<int64_t>(q.outer, 65535));
+    const uint64_t want_total = (uint64_t)sms * 8;
+    const uint64_t gx = std::max<uint64_t>(1, std::min<uint64_t>((items + kThr - 1) / kThr,
+                                                                  (want_total + gy - 1) / gy));
+    return dim3((unsigned)gx, gy);
+}
+
+template <bool STATS>
+struct DsL {
+    template <int B, bool A, int S, int Z> struct L {
+        static void run(const QArgs& a, cudaStream_t st) {
+            const QSpec& q = a.q;
+            const dim3 grid = ds_grid(q, sm_count());
+            const int lcpr = log2_exact(q.C / 8), lg = log2_exact(q.g);
+            Partial* partials = static_cast<Partial*>(a.ws);
+            if (q.axis == KVQ_GROUP_ALONG_T)
+                ds_kernel<B, A, true, kRpt, STATS, S, Z><<<grid, kThr, 0, st>>>(a, lcpr, lg, partials);
+            else
+                ds_kernel<B, A, false, kRpt, STATS, S, Z><<<grid, kThr, 0, st>>>(a, lcpr, lg, partials);
+        }
+    };
+};
+
+}  // namespace
+
+// ---- entry points (see kvq_internal.h)
+
+bool staged_quantize_supported(const QSpec& q)
+{
+    return q.axis == KVQ_GROUP_ALONG_T ? staged_t_ok(q) : staged_c_ok(q);
+}
+
+bool staged_quantize(const QArgs& a, cudaStream_t st)
+{
+    const QSpec& q = a.q;
+    if (q.axis == KVQ_GROUP_ALONG_T && staged_t_ok(q)) { by_meta<SqT>(a, st); return true; }
+    if (q.axis == KVQ_GROUP_ALONG_C && staged_c_ok(q)) { by_meta<SqC>(a, st); return true; }
+    return false;
+}
+
+bool stream_dequant_supported(const QSpec& q, int out_dt) { return out_dt == KVQ_BF16 && ds_ok(q) && q.Tq > 0; }
+
+cudaError_t stream_dequantize(const QArgs& a, cudaStream_t st)
+{
+    by_meta<DsL<false>::L>(a, st);
+    return cudaGetLastError();
+}
+
+int64_t stream_stats_blocks(const QSpec& q, int sms)
+{
+    if (!ds_ok(q)) return -1;
+    const dim3 g = ds_grid(q, sms);
+    return (int64_t)g.x * g.y;
+}
+
+cudaError_t stream_error_stats(const QArgs& a, void* partials, cudaStream_t st)
+{
+    QArgs b = a;
+    b.ws = partials;
+    by_meta<DsL<true>::L>(b, st);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq
