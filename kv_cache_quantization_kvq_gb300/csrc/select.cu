@@ -34,7 +34,7 @@ constexpr int kCols = 4 * kThreads;    // columns per chunk
 constexpr int kBins1 = 4096, kBins2 = 4096, kBins3 = 256;
 
 struct SelectLayout {
-    size_t scores, hist1, hist2, hist3, state, counts, total;
+    size_t scores, hist1, hist2, hist3, state, counts, ccount, done, cand, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -50,6 +50,9 @@ SelectLayout layout(int64_t heads, int64_t T)
     L.hist3 = off;  off = align256(off + (size_t)heads * kBins3 * 4);
     L.state = off;  off = align256(off + (size_t)heads * 4 * 4);
     L.counts = off; off = align256(off + (size_t)(heads * nchunks) * 2 * 4);
+    L.ccount = off; off = align256(off + (size_t)heads * 4);
+    L.done = off;   off = align256(off + (size_t)heads * 4);
+    L.cand = off;   off = align256(off + (size_t)(heads * T) * 8);     // room for every key
     L.total = off;
     return L;
 }
@@ -59,13 +62,15 @@ __device__ __forceinline__ uint32_t score_key(float s) { return float_key(s == 0
 
 // ---------------------------------------------------------------- scores
 
-template <bool VEC>
+template <bool VEC, bool HIST>
 __global__ void __launch_bounds__(kThreads)
 colsum_hist_kernel(const SelectArgs a, int64_t rs, float* scores, uint32_t* hist1)
 {
-    __shared__ uint32_t sh[kBins1];
-    for (int i = threadIdx.x; i < kBins1; i += kThreads) sh[i] = 0;
-    __syncthreads();
+    __shared__ uint32_t sh[HIST ? kBins1 : 1];
+    if (HIST) {
+        for (int i = threadIdx.x; i < kBins1; i += kThreads) sh[i] = 0;
+        __syncthreads();
+    }
     const int64_t h = blockIdx.y;
     const int64_t T = a.T;
     const int64_t col0 = (int64_t)blockIdx.x * kCols + threadIdx.x * 4;
@@ -111,13 +116,134 @@ colsum_hist_kernel(const SelectArgs a, int64_t rs, float* scores, uint32_t* hist
         const int64_t col = col0 + j;
         if (col < T) {
             if (!VEC) scores[h * T + col] = s[j];
-            if (col < rs) atomicAdd(&sh[score_key(s[j]) >> 20], 1u);
+            if (HIST && col < rs) atomicAdd(&sh[score_key(s[j]) >> 20], 1u);
         }
     }
     if (VEC && col0 < T) *reinterpret_cast<float4*>(scores + h * T + col0) = make_float4(s[0], s[1], s[2], s[3]);
+    if (HIST) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < kBins1; i += kThreads)
+            if (sh[i]) atomicAdd(&hist1[h * kBins1 + i], sh[i]);
+    }
+}
+
+// Column sums for the candidate path: CTA (bx, h) walks chunks bx, bx+gx, ...
+// of head h, so its shared-memory histogram of candidate keys (top 12 bits)
+// is flushed once; the last CTA of the head to finish picks the level-1 bin
+// b1 holding the k-th largest key (state[h] = {b1, keys above b1}).
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads)
+colsum_bin1_kernel(const SelectArgs a, int64_t rs, int64_t k, float* scores, uint32_t* hist1, uint32_t* done,
+                   uint32_t* state, uint32_t* ccount, bool want_bin)
+{
+    __shared__ uint32_t sh[kBins1];
+    __shared__ int wsum[kThreads / 32];
+    __shared__ bool s_last;
+    for (int i = threadIdx.x; i < kBins1; i += kThreads) sh[i] = 0;
+    __syncthreads();
+    const int64_t h = blockIdx.y;
+    const int64_t T = a.T;
+    const int64_t nr = a.nrows;
+    const float* base = a.hist + (h * a.steps + a.row0) * T;
+    const int64_t nchunks = (T + kCols - 1) / kCols;
+    for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
+        const int64_t col0 = chunk * kCols + threadIdx.x * 4;
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (VEC) {
+            if (col0 < T) {
+                const float4* p = reinterpret_cast<const float4*>(base + col0);
+                const int64_t rstride = T / 4;
+                int64_t t = 0;
+                for (; t + 8 <= nr; t += 8) {
+                    float4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v[u] = __ldcs(p + (t + u) * rstride);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        s[0] = __fadd_rn(s[0], v[u].x);
+                        s[1] = __fadd_rn(s[1], v[u].y);
+                        s[2] = __fadd_rn(s[2], v[u].z);
+                        s[3] = __fadd_rn(s[3], v[u].w);
+                    }
+                }
+                for (; t < nr; ++t) {
+                    const float4 v = __ldcs(p + t * rstride);
+                    s[0] = __fadd_rn(s[0], v.x);
+                    s[1] = __fadd_rn(s[1], v.y);
+                    s[2] = __fadd_rn(s[2], v.z);
+                    s[3] = __fadd_rn(s[3], v.w);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t col = col0 + j;
+                if (col < T)
+                    for (int64_t t = 0; t < nr; ++t) s[j] = __fadd_rn(s[j], base[t * T + col]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (a.divide) s[j] = __fdiv_rn(s[j], (float)nr);
+            const int64_t col = col0 + j;
+            if (col < T) {
+                if (!VEC) scores[h * T + col] = s[j];
+                if (want_bin && col < rs) atomicAdd(&sh[score_key(s[j]) >> 20], 1u);
+            }
+        }
+        if (VEC && col0 < T) *reinterpret_cast<float4*>(scores + h * T + col0) = make_float4(s[0], s[1], s[2], s[3]);
+    }
+    if (!want_bin) return;
     __syncthreads();
     for (int i = threadIdx.x; i < kBins1; i += kThreads)
         if (sh[i]) atomicAdd(&hist1[h * kBins1 + i], sh[i]);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&done[h], 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // last CTA of the head: scan the histogram from the top bin down
+    const int bpt = kBins1 / kThreads;              // 16
+    const int top = kBins1 - 1 - (int)threadIdx.x * bpt;
+    int cnt[kBins1 / kThreads];
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < kBins1 / kThreads; ++j) { cnt[j] = (int)__ldcg(hist1 + h * kBins1 + top - j); local += cnt[j]; }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int y = lane < kThreads / 32 ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < kThreads / 32; o <<= 1) {
+            const int z = __shfl_up_sync(0xFFFFFFFFu, y, o);
+            if (lane >= o) y += z;
+        }
+        if (lane < kThreads / 32) wsum[lane] = y;
+    }
+    __syncthreads();
+    const int64_t incl = x + (w > 0 ? wsum[w - 1] : 0);
+    const int64_t excl = incl - local;
+    if (excl < k && k <= incl) {
+        int64_t acc = excl;
+#pragma unroll
+        for (int j = 0; j < kBins1 / kThreads; ++j) {
+            if (acc + cnt[j] >= k) {
+                state[h * 4 + 0] = (uint32_t)(top - j);
+                state[h * 4 + 1] = (uint32_t)acc;
+                break;
+            }
+            acc += cnt[j];
+        }
+    }
+    if (threadIdx.x == 0) ccount[h] = 0;
 }
 
 // ---------------------------------------------------------------- block scans
@@ -337,6 +463,223 @@ emit_kernel(const float* scores, int64_t T, int64_t rs, int64_t K, int64_t k, in
         }
 }
 
+// ---------------------------------------------------------------- candidate select
+//
+// After the level-1 histogram (top 12 key bits, built by colsum_bin1) the
+// k-th largest key lies in one bin b1; only keys in bins >= b1 can be kept.
+//   colsum_bin1     column sums plus the level-1 histogram; the last CTA of
+//                   each head picks b1 and the count of keys above it;
+//   gather_kernel   one pass over the scores: candidates (bin >= b1) are
+//                   appended to the head's list (one atomic per CTA);
+//   finish_kernel   one CTA per head: levels 2 and 3 (12 + 8 bits) over the
+//                   candidates of bin b1 give the exact k-th key T* and the
+//                   number of ties to keep; the kept indices are marked in a
+//                   shared-memory bitmap over [0, T) -- ties in index order --
+//                   and written out by a scan of the bitmap, i.e. ascending.
+constexpr int kFinThreads = 1024;
+constexpr int64_t kBitmapMaxT = int64_t(1) << 19;     // two shared-memory bitmaps of T bits (128 KB)
+
+__global__ void __launch_bounds__(kThreads)
+gather_kernel(const float* scores, int64_t T, int64_t rs, const uint32_t* state, uint32_t* ccount, uint2* cand,
+              int64_t cap, bool vec)
+{
+    __shared__ uint32_t s_base;
+    const int64_t h = blockIdx.y;
+    const uint32_t b1 = state[h * 4 + 0];
+    const int64_t col0 = (int64_t)blockIdx.x * kCols + threadIdx.x * 4;
+    float v[4];
+    if (vec && col0 + 3 < rs) {
+        const float4 f = *reinterpret_cast<const float4*>(scores + h * T + col0);
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = col0 + j < rs ? scores[h * T + col0 + j] : 0.0f;
+    }
+    uint32_t key[4];
+    int n = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        key[j] = score_key(v[j]);
+        n += (col0 + j < rs) && (key[j] >> 20) >= b1;
+    }
+    int total;
+    const int excl = block_excl_scan(n, total);
+    if (total == 0) return;                               // uniform
+    if (threadIdx.x == 0) s_base = atomicAdd(&ccount[h], (uint32_t)total);
+    __syncthreads();
+    uint32_t pos = s_base + (uint32_t)excl;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int64_t col = col0 + j;
+        if (col < rs && (key[j] >> 20) >= b1) {
+            if (pos < cap) cand[h * cap + pos] = make_uint2(key[j], (uint32_t)col);
+            ++pos;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kFinThreads)
+finish_kernel(int64_t T, int64_t rs, int64_t k, int64_t K, const uint32_t* state, const uint32_t* ccount,
+              const uint2* cand, int64_t cap, int32_t* keep)
+{
+    extern __shared__ uint32_t bitmap[];                 // ceil(T/32) words, later tie bits reuse hist
+    __shared__ uint32_t hist[kBins2];
+    __shared__ int wsum[32];
+    __shared__ uint32_t s_val[2];
+    const int64_t h = blockIdx.x;
+    const uint32_t b1 = state[h * 4 + 0];
+    const int64_t above = (int64_t)state[h * 4 + 1];
+    const int64_t m = min((int64_t)ccount[h], cap);
+    const uint2* ch = cand + h * cap;
+    const int nwords = (int)((T + 31) / 32);
+    int32_t* kh = keep + h * K;
+
+    // levels 2 and 3 among the candidates of bin b1
+    uint32_t prefix = b1, rem = (uint32_t)(k - above);
+    for (int level = 2; level <= 3; ++level) {
+        const int nbins = level == 2 ? kBins2 : kBins3;
+        for (int b = threadIdx.x; b < nbins; b += kFinThreads) hist[b] = 0;
+        __syncthreads();
+        for (int64_t i = threadIdx.x; i < m; i += kFinThreads) {
+            const uint32_t key = ch[i].x;
+            if (level == 2) { if ((key >> 20) == prefix) atomicAdd(&hist[(key >> 8) & 0xFFFu], 1u); }
+            else if ((key >> 8) == prefix) atomicAdd(&hist[key & 0xFFu], 1u);
+        }
+        __syncthreads();
+        const int bpt = (nbins + kFinThreads - 1) / kFinThreads;
+        const int top = nbins - 1 - (int)threadIdx.x * bpt;
+        int local = 0;
+        for (int j = 0; j < bpt; ++j)
+            if (top - j >= 0) local += (int)hist[top - j];
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        int x = local;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int y = wsum[lane];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int z = __shfl_up_sync(0xFFFFFFFFu, y, o);
+                if (lane >= o) y += z;
+            }
+            wsum[lane] = y;
+        }
+        __syncthreads();
+        const int incl = x + (w > 0 ? wsum[w - 1] : 0);
+        const int excl = incl - local;
+        if (excl < (int)rem && (int)rem <= incl) {
+            int acc = excl;
+            for (int j = 0; j < bpt; ++j) {
+                const int b = top - j;
+                if (b < 0) break;
+                if (acc + (int)hist[b] >= (int)rem) {
+                    s_val[0] = (prefix << (level == 2 ? 12 : 8)) | (uint32_t)b;
+                    s_val[1] = rem - (uint32_t)acc;
+                    break;
+                }
+                acc += (int)hist[b];
+            }
+        }
+        __syncthreads();
+        prefix = s_val[0];
+        rem = s_val[1];
+        __syncthreads();
+    }
+    const uint32_t kth = prefix;
+    const uint32_t need = rem;
+
+    // bitmap of kept candidates: keys above T*, then the lowest-index ties
+    for (int i = threadIdx.x; i < nwords; i += kFinThreads) bitmap[i] = 0;
+    __syncthreads();
+    uint32_t* ties = bitmap + nwords;                    // second bitmap for the ties
+    for (int i = threadIdx.x; i < nwords; i += kFinThreads) ties[i] = 0;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < m; i += kFinThreads) {
+        const uint2 c = ch[i];
+        if (c.x > kth) atomicOr(&bitmap[c.y >> 5], 1u << (c.y & 31));
+        else if (c.x == kth) atomicOr(&ties[c.y >> 5], 1u << (c.y & 31));
+    }
+    __syncthreads();
+    // keep the first `need` tie bits in index order
+    {
+        const int wpt = (nwords + kFinThreads - 1) / kFinThreads;
+        const int w0 = (int)threadIdx.x * wpt;
+        int local = 0;
+        for (int j = 0; j < wpt; ++j)
+            if (w0 + j < nwords) local += __popc(ties[w0 + j]);
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        int x = local;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int y = wsum[lane];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int z = __shfl_up_sync(0xFFFFFFFFu, y, o);
+                if (lane >= o) y += z;
+            }
+            wsum[lane] = y;
+        }
+        __syncthreads();
+        int before = x - local + (w > 0 ? wsum[w - 1] : 0);
+        for (int j = 0; j < wpt; ++j) {
+            if (w0 + j >= nwords) break;
+            uint32_t tw = ties[w0 + j];
+            while (tw) {
+                const int bit = __ffs(tw) - 1;
+                tw &= tw - 1;
+                if ((uint32_t)before < need) bitmap[w0 + j] |= 1u << bit;
+                ++before;
+            }
+        }
+        __syncthreads();
+    }
+    // scan the kept bitmap in index order and write the indices ascending
+    {
+        const int wpt = (nwords + kFinThreads - 1) / kFinThreads;
+        const int w0 = (int)threadIdx.x * wpt;
+        int local = 0;
+        for (int j = 0; j < wpt; ++j)
+            if (w0 + j < nwords) local += __popc(bitmap[w0 + j]);
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        int x = local;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int y = wsum[lane];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int z = __shfl_up_sync(0xFFFFFFFFu, y, o);
+                if (lane >= o) y += z;
+            }
+            wsum[lane] = y;
+        }
+        __syncthreads();
+        int pos = x - local + (w > 0 ? wsum[w - 1] : 0);
+        for (int j = 0; j < wpt; ++j) {
+            if (w0 + j >= nwords) break;
+            uint32_t bw = bitmap[w0 + j];
+            while (bw) {
+                const int bit = __ffs(bw) - 1;
+                bw &= bw - 1;
+                if (pos < k) kh[pos] = (int32_t)((w0 + j) * 32 + bit);
+                ++pos;
+            }
+        }
+    }
+    // the recent window follows the heavy hitters
+    for (int64_t i = rs + threadIdx.x; i < T; i += kFinThreads) kh[k + (i - rs)] = (int32_t)i;
+}
+
 }  // namespace
 
 size_t select_workspace(int64_t heads, int64_t T) { return layout(heads, T).total; }
@@ -362,11 +705,40 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st)
     const int64_t nchunks = (T + kCols - 1) / kCols;
     const dim3 grid((unsigned)nchunks, (unsigned)H);
 
+    const bool vec = (T % 4 == 0) && ((uintptr_t)a.hist % 16 == 0) && ((uintptr_t)scores % 16 == 0);
+    // candidates path: level-1 histogram and bin in the column sum, then gather + finish
+    if (T <= kBitmapMaxT) {
+        uint32_t* ccount = reinterpret_cast<uint32_t*>(ws + L.ccount);
+        uint32_t* done = reinterpret_cast<uint32_t*>(ws + L.done);
+        uint2* cand = reinterpret_cast<uint2*>(ws + L.cand);
+        const bool want_bin = mode == 2;
+        if (want_bin) {
+            cudaError_t e = cudaMemsetAsync(ws + L.hist1, 0, (size_t)H * kBins1 * 4, st);
+            if (e == cudaSuccess) e = cudaMemsetAsync(done, 0, (size_t)H * 4, st);
+            if (e != cudaSuccess) return e;
+        }
+        const int64_t per_head = std::max<int64_t>(1, std::min<int64_t>(nchunks, ((int64_t)sm_count() * 4 + H - 1) / H));
+        const dim3 cgrid((unsigned)per_head, (unsigned)H);
+        if (vec) colsum_bin1_kernel<true><<<cgrid, kThreads, 0, st>>>(a, rs, k, scores, hist1, done, state, ccount, want_bin);
+        else colsum_bin1_kernel<false><<<cgrid, kThreads, 0, st>>>(a, rs, k, scores, hist1, done, state, ccount, want_bin);
+        if (mode == 2) {
+            gather_kernel<<<grid, kThreads, 0, st>>>(scores, T, rs, state, ccount, cand, T, vec);
+            const size_t smem = (size_t)2 * ((T + 31) / 32) * 4;
+            static size_t attr = 0;
+            if (smem > attr) {                       // static + dynamic may exceed the 48 KB default
+                cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                attr = smem;
+            }
+            finish_kernel<<<(unsigned)H, kFinThreads, smem, st>>>(T, rs, k, K, state, ccount, cand, T, a.keep);
+        } else {
+            emit_kernel<<<grid, kThreads, 0, st>>>(scores, T, rs, K, k, mode, state, counts, a.keep);
+        }
+        return cudaGetLastError();
+    }
     cudaError_t e = cudaMemsetAsync(ws + L.hist1, 0, L.counts - L.hist1, st);
     if (e != cudaSuccess) return e;
-    const bool vec = (T % 4 == 0) && ((uintptr_t)a.hist % 16 == 0) && ((uintptr_t)scores % 16 == 0);
-    if (vec) colsum_hist_kernel<true><<<grid, kThreads, 0, st>>>(a, rs, scores, hist1);
-    else colsum_hist_kernel<false><<<grid, kThreads, 0, st>>>(a, rs, scores, hist1);
+    if (vec) colsum_hist_kernel<true, true><<<grid, kThreads, 0, st>>>(a, rs, scores, hist1);
+    else colsum_hist_kernel<false, true><<<grid, kThreads, 0, st>>>(a, rs, scores, hist1);
     if (mode == 2) {
         select_digit_kernel<<<(unsigned)H, 1024, 0, st>>>(hist1, kBins1, 12, 1, k, state);
         refine_hist_kernel<<<grid, kThreads, 0, st>>>(scores, T, rs, state, 2, hist2);
