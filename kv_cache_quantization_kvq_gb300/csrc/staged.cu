@@ -260,6 +260,202 @@ sq_t_kernel(const QArgs a)
 }
 
 // ======================================================================
+// groups along T, warp-specialised (C = 128, g in {16, 32, 64}).  A producer
+// warp keeps a ring of kWStages stages full with bulk copies; each stage is
+// one group tile [g tokens x 128 channels] and belongs to one consumer warp
+// for the whole of its processing: lane = 8 channels x every other token of
+// the tile, so a group's min / max is one shuffle away and no block-wide
+// barrier is ever taken.  Stage s is handed back to the producer by one
+// arrival on empty[s].
+// ======================================================================
+constexpr int kWConsumers = 8;
+constexpr int kWStages = 13;
+constexpr int kWThreads = (kWConsumers + 1) * 32;
+constexpr int kWSmem = kWStages * kStageBytes + 2 * kWStages * 8;
+
+template <int BITS, bool ASYM, int G, int SDT, int ZDT>
+__global__ void __launch_bounds__(kWThreads, 1)
+wq_t_kernel(const QArgs a)
+{
+    constexpr int C = 128;
+    constexpr int RPL = G / 2;                          // rows per lane in a full tile
+    constexpr uint32_t kRowB = C * 2;                   // bytes of one bf16 row
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWStages * kStageBytes);
+    uint64_t* empty = full + kWStages;
+
+    const QSpec& q = a.q;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ng = (uint32_t)q.ngroups;
+    const uint32_t nres = (uint32_t)((q.R + G - 1) / G);
+    const uint32_t per_o = ng + nres;
+    const uint32_t nchunks = (uint32_t)q.outer * per_o;   // < 2^31, checked by the dispatcher
+    const uint32_t Tq32 = (uint32_t)q.Tq, T32 = (uint32_t)q.T;
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    auto geom = [&](uint32_t c, uint32_t& o, uint32_t& k, uint32_t& row0, int& nrows, bool& res) {
+        o = c / per_o;
+        k = c - o * per_o;
+        res = k >= ng;
+        row0 = res ? Tq32 + (k - ng) * (uint32_t)G : k * (uint32_t)G;
+        const uint32_t end = res ? T32 : Tq32;
+        nrows = (int)min((uint32_t)G, end - row0);
+    };
+    const uint32_t first = blockIdx.x, step = gridDim.x;
+
+    if (warp == kWConsumers) {
+        // ---- producer: one lane issues every copy of this CTA
+        if (lane != 0) return;
+        uint32_t n = 0;
+        for (;; ++n) {
+            const uint32_t c = first + n * step;
+            if (c >= nchunks) break;
+            const int s = (int)(n % kWStages);
+            if (n >= (uint32_t)kWStages && !mbar_wait(&empty[s], ((n / kWStages) - 1) & 1u)) break;
+            uint32_t o, k, row0; int nrows; bool res;
+            geom(c, o, k, row0, nrows, res);
+            const uint32_t bytes = (uint32_t)nrows * kRowB;
+            mbar_expect_tx(&full[s], bytes);
+            bulk_g2s(smem + s * kStageBytes, x + ((uint64_t)o * T32 + row0) * C, bytes, &full[s]);
+        }
+        // every copy issued must land before the CTA may exit
+        for (uint32_t i = n > (uint32_t)kWStages ? n - kWStages : 0; i < n; ++i)
+            mbar_wait(&full[i % kWStages], (i / kWStages) & 1u);
+        return;
+    }
+
+    // ---- consumers
+    const int c8 = lane & 15, h = lane >> 4;
+    const int off = q.is_signed ? (1 << (BITS - 1)) : 0;
+    const int lo_c = q.qmin + off, hi_c = q.qmax + off;
+    uint8_t* codes = static_cast<uint8_t*>(a.codes);
+    constexpr uint32_t kCodeRowB = C * BITS / 8;
+    for (uint32_t j = warp;; j += kWConsumers) {
+        const uint32_t c = first + j * step;
+        if (c >= nchunks) break;
+        const int s = (int)(j % kWStages);
+        if (!mbar_wait(&full[s], (j / kWStages) & 1u)) return;   // recorded in g_kvq_wait_timeouts
+        const unsigned char* tile = smem + s * kStageBytes + c8 * 16 + h * kRowB;
+        uint32_t o, k, row0; int nrows; bool res;
+        geom(c, o, k, row0, nrows, res);
+        const bool whole = nrows == G;
+        if (res) {
+            __nv_bfloat16* rp = static_cast<__nv_bfloat16*>(a.resid) +
+                                (((uint64_t)o * q.R + (row0 - Tq32) + h) * C + c8 * 8);
+#pragma unroll 4
+            for (int i = 0; i < RPL; ++i)
+                if (2 * i + h < nrows)
+                    *reinterpret_cast<uint4*>(rp + (uint64_t)i * 2 * C) = *reinterpret_cast<const uint4*>(tile + i * 2 * kRowB);
+        } else {
+            // group min / max (abs-max when symmetric) over the lane's rows, then over both halves
+            uint32_t mn[4], mx[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) { mn[p] = kBfPosInf2; mx[p] = ASYM ? kBfNegInf2 : 0u; }
+            auto fold = [&](const uint4& w) {     // per channel pair
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    if (ASYM) { mn[p] = bmin2(mn[p], ws[p]); mx[p] = bmax2(mx[p], ws[p]); }
+                    else mx[p] = bmax2(mx[p], babs2(ws[p]));
+                }
+            };
+            if (whole) {
+#pragma unroll 8
+                for (int i = 0; i < RPL; ++i) fold(*reinterpret_cast<const uint4*>(tile + i * 2 * kRowB));
+            } else {
+#pragma unroll 4
+                for (int i = 0; i < RPL; ++i)
+                    if (2 * i + h < nrows) fold(*reinterpret_cast<const uint4*>(tile + i * 2 * kRowB));
+            }
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                if (ASYM) mn[p] = bmin2(mn[p], __shfl_xor_sync(0xFFFFFFFFu, mn[p], 16));
+                mx[p] = bmax2(mx[p], __shfl_xor_sync(0xFFFFFFFFu, mx[p], 16));
+            }
+            // lane half h derives the constants of channels 4h .. 4h+3 of its 8
+            const uint32_t wmn[2] = {h ? mn[2] : mn[0], h ? mn[3] : mn[1]};
+            const uint32_t wmx[2] = {h ? mx[2] : mx[0], h ? mx[3] : mx[1]};
+            float os[4], oi[4], oz[4];
+            int32_t ozo[4];
+            bool fast = true;
+            const int64_t mi = ((int64_t)o * ng + k) * C + c8 * 8 + 4 * h;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const uint32_t m0 = wmn[jj >> 1], m1 = wmx[jj >> 1];
+                const float fmn = (jj & 1) ? hi_f(m0) : lo_f(m0);
+                const float fmx = (jj & 1) ? hi_f(m1) : lo_f(m1);
+                const GroupC gc = make_group<ASYM>(fmn, fmx, q, off);
+                write_meta_t<SDT, ZDT>(a, mi + jj, gc);
+                os[jj] = gc.s; oi[jj] = gc.inv; oz[jj] = gc.zp; ozo[jj] = gc.zoff;
+                fast = fast && gc.fast;
+            }
+            const bool all_fast = __all_sync(0xFFFFFFFFu, fast);
+            // the partner half's four channels
+            float ps[4], pi[4];
+            int32_t pzo[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                ps[jj] = __shfl_xor_sync(0xFFFFFFFFu, os[jj], 16);
+                pi[jj] = __shfl_xor_sync(0xFFFFFFFFu, oi[jj], 16);
+                pzo[jj] = __shfl_xor_sync(0xFFFFFFFFu, ozo[jj], 16);
+            }
+            float s8[8], i8[8];
+            int32_t zo[8];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                s8[jj] = h ? ps[jj] : os[jj];       s8[jj + 4] = h ? os[jj] : ps[jj];
+                i8[jj] = h ? pi[jj] : oi[jj];       i8[jj + 4] = h ? oi[jj] : pi[jj];
+                zo[jj] = h ? pzo[jj] : ozo[jj];     zo[jj + 4] = h ? ozo[jj] : pzo[jj];
+            }
+            uint8_t* cp = codes + ((uint64_t)o * Tq32 + row0 + h) * kCodeRowB + (uint32_t)c8 * BITS;
+            if (all_fast) {
+                QuotK kq[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    kq[p].ns = pk(-s8[2 * p], -s8[2 * p + 1]);
+                    kq[p].inv = pk(i8[2 * p], i8[2 * p + 1]);
+                }
+                auto emit = [&](int i) {
+                    uint32_t cc[8];
+                    codes8_fast<ASYM>(*reinterpret_cast<const uint4*>(tile + i * 2 * kRowB), kq, zo, lo_c, hi_c, cc);
+                    store_codes<BITS>(cp + (uint64_t)i * 2 * kCodeRowB, finish_word<BITS>(cc, q.is_signed));
+                };
+                if (whole) {
+#pragma unroll 4
+                    for (int i = 0; i < RPL; ++i) emit(i);
+                } else {
+                    for (int i = 0; i < RPL; ++i)
+                        if (2 * i + h < nrows) emit(i);
+                }
+            } else {
+                float pz[4], z8[8];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) pz[jj] = __shfl_xor_sync(0xFFFFFFFFu, oz[jj], 16);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) { z8[jj] = h ? pz[jj] : oz[jj]; z8[jj + 4] = h ? oz[jj] : pz[jj]; }
+                for (int i = 0; i < RPL; ++i)
+                    if (2 * i + h < nrows) {
+                        uint32_t cc[8];
+                        codes8_slow<ASYM>(*reinterpret_cast<const uint4*>(tile + i * 2 * kRowB), s8, z8, q, off, cc);
+                        store_codes<BITS>(cp + (uint64_t)i * 2 * kCodeRowB, finish_word<BITS>(cc, q.is_signed));
+                    }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+// ======================================================================
 // groups along C: chunk = 8192/C whole token rows; thread = 32 channels
 // ======================================================================
 template <int BITS, bool ASYM, int G, int SDT, int ZDT>
@@ -541,10 +737,27 @@ bool staged_c_ok(const QSpec& q) {
     return q.C % g == 0 && (g == 32 || g == 64 || g == 128);
 }
 
+template <int BITS, bool ASYM, int G, int SDT, int ZDT>
+void wq_t_launch(const QArgs& a, uint64_t nchunks, cudaStream_t st) {
+    const unsigned grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(nchunks, (uint64_t)sm_count()));
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(wq_t_kernel<BITS, ASYM, G, SDT, ZDT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
+        attr = true;
+    }
+    wq_t_kernel<BITS, ASYM, G, SDT, ZDT><<<grid, kWThreads, kWSmem, st>>>(a);
+}
+
 template <int BITS, bool ASYM, int SDT, int ZDT>
 void sq_t_launch(const QArgs& a, cudaStream_t st) {
     const QSpec& q = a.q;
     const uint64_t nchunks = (uint64_t)q.outer * (q.ngroups + (q.R + q.g - 1) / q.g);
+    switch (q.g) {
+    case 16: wq_t_launch<BITS, ASYM, 16, SDT, ZDT>(a, nchunks, st); return;
+    case 32: wq_t_launch<BITS, ASYM, 32, SDT, ZDT>(a, nchunks, st); return;
+    case 64: wq_t_launch<BITS, ASYM, 64, SDT, ZDT>(a, nchunks, st); return;
+    default: break;
+    }
     const unsigned grid = staged_grid(sm_count(), nchunks);
     ensure_smem(sq_t_kernel<BITS, ASYM, 128, SDT, ZDT>);
     sq_t_kernel<BITS, ASYM, 128, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a);

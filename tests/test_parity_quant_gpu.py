@@ -184,6 +184,47 @@ def test_along_t_partial_channel_block(b, C):
     check_case(b, xin, O.BF16, sym(8, axis=O.ALONG_T, group=0, residual=4))
 
 
+# head_dim 128 with bf16 input: the warp-specialised group-tile kernel (g in
+# {16, 32, 64}) and the block-tile kernel (other g <= 64), for every metadata
+# layout they specialise (bf16 scale + zero, f32 scale + int8 zero, bf16 or
+# f32 scale alone); ragged last quantized group, ragged residual tile.
+HD128_T_CASES = []
+for bits, g in itertools.product((8, 4, 2), (16, 32, 64, 48)):
+    HD128_T_CASES.append(("sym", bits, g, O.BF16, O.NONE, None))
+    HD128_T_CASES.append(("sym", bits, g, O.F32, O.NONE, None))
+    for qr in asym_ranges(bits):
+        HD128_T_CASES.append(("asym", bits, g, O.BF16, O.BF16, qr))
+        HD128_T_CASES.append(("asym", bits, g, O.F32, O.I8, qr))
+
+
+@pytest.mark.parametrize("case", HD128_T_CASES, ids=str)
+def test_along_t_head_dim_128(b, case):
+    mode, bits, g, sdt, zdt, qr = case
+    rng = np.random.default_rng(zlib.crc32(repr(case).encode()))
+    xin = make_input(rng, (3, 301, 128), O.BF16)
+    if mode == "sym":
+        oq = sym(bits, axis=O.ALONG_T, group=g, residual=13, scale_dtype=sdt)
+    else:
+        oq = O.QParams.asym(bits, qr[0], qr[1], axis=O.ALONG_T, group=g, residual=13, scale_dtype=sdt,
+                            zero_dtype=zdt)
+    check_case(b, xin, O.BF16, oq)
+
+
+@pytest.mark.parametrize("kind", ["zeros", "ties", "wide", "const"])
+@pytest.mark.parametrize("T,R", [(200, 0), (150, 64), (40, 128), (64, 70)])
+def test_along_t_head_dim_128_values_and_lengths(b, kind, T, R):
+    """Value kinds that force the IEEE-division fallback inside a tile
+    ("wide"), exact ties, constant groups; no residual, a residual shorter
+    than, equal to and longer than one group tile."""
+    rng = np.random.default_rng(T * 7 + R + len(kind))
+    xin = make_input(rng, (2, T, 128), O.BF16, kind)
+    for oq in (O.QParams.asym(4, 0, 15, axis=O.ALONG_T, group=64, residual=R, scale_dtype=O.BF16,
+                              zero_dtype=O.BF16),
+               O.QParams.asym(2, -2, 1, axis=O.ALONG_T, group=32, residual=R, zero_dtype=O.I8),
+               sym(8, axis=O.ALONG_T, group=16, residual=R, scale_dtype=O.BF16)):
+        check_case(b, xin, O.BF16, oq)
+
+
 # ---------------------------------------------------------------- edge cases
 
 
