@@ -107,6 +107,12 @@ kvq_status make_spec(const kvq_shape* sh, int x_dt, const kvq_qparams* p, kvq::Q
     q.is_signed = (p->mode == KVQ_SYM || p->qmin < 0) ? 1 : 0;
     q.lo = (float)q.qmin;
     q.hi = (float)q.qmax;
+    {
+        // the group constants divide by this integer; its correctly rounded
+        // reciprocal drives the exact fast quotient for ranges 1..255
+        const int qr = p->mode == KVQ_SYM ? q.qmax : q.qmax - q.qmin;
+        q.inv_qr = (qr >= 1 && qr <= 255) ? 1.0f / (float)qr : 0.0f;
+    }
     q.aligned = 1;
     return KVQ_OK;
 }

@@ -18,41 +18,66 @@ struct GroupC {
     float s, inv, zp;   // scale and zero point as stored, RN(1/s)
     int32_t zoff;       // clean code = bits(rint(q)+1.5*2^23) + zoff
     bool fast;          // the fast quotient's preconditions hold
+    bool lo_ok;         // fast, and no code of the group falls below the clip floor
 };
 
-// off = 2^(bits-1) for signed codes (offset binary in registers), else 0
+// off = 2^(bits-1) for signed codes (offset binary in registers), else 0.
+// The two divisions of the group constants -- range by the integer qmax -
+// qmin (or abs-max by qmax) and min by the stored scale -- are the exact
+// IEEE quotients, taken by the reciprocal + remainder method when its
+// preconditions hold and by __fdiv_rn otherwise.  Codes are monotone in x, so
+// the group's lowest code is the code of its minimum: when that one is not
+// below the floor no element needs the lower clip.
 template <bool ASYM>
 __device__ __forceinline__ GroupC make_group(float mn, float mx, const QSpec& q, int off) {
     GroupC g;
-    Meta m;
-    float amag;
+    float amag, s;
     if (ASYM) {
-        m = meta_asym(mn, mx, q);
+        const float rng = fmaxf(__fsub_rn(mx, mn), range_floor());
+        const float qr = (float)(q.qmax - q.qmin);
+        s = (q.inv_qr > 0.0f && rng <= 0x1p127f) ? quot1(rng, qr, q.inv_qr) : __fdiv_rn(rng, qr);
         amag = fmaxf(fabsf(mn), fabsf(mx));
     } else {
-        m = meta_sym(mx, q);      // mx carries the abs-max
+        const float am = fmaxf(mx, range_floor());     // mx carries the abs-max
+        s = (q.inv_qr > 0.0f && am <= 0x1p127f) ? quot1(am, (float)q.qmax, q.inv_qr) : __fdiv_rn(am, (float)q.qmax);
         amag = mx;
     }
-    g.s = m.s;
-    g.zp = m.z;
-    g.inv = __frcp_rn(m.s);
-    g.fast = quot_ok(m.s, g.inv, amag) && fabsf(m.z) < 0x1p21f;
-    g.zoff = (ASYM ? (int32_t)m.z : 0) + off - (int32_t)kMagicBits;
+    g.s = scale_as_stored(s, q.scale_dt);
+    g.inv = __frcp_rn(g.s);
+    const bool qok = quot_ok(g.s, g.inv, amag);
+    if (ASYM) {
+        // min / s by the fast quotient only where it is exact (|min| >= 2^-100 or 0)
+        const bool mn_ok = qok && (fabsf(mn) >= 0x1p-100f || mn == 0.0f);
+        const float a = mn_ok ? quot1(mn, g.s, g.inv) : __fdiv_rn(mn, g.s);
+        g.zp = zero_as_stored(rintf(__fsub_rn((float)q.qmin, a)), q.zero_dt);
+        g.fast = qok && fabsf(g.zp) < 0x1p21f;
+        g.zoff = (int32_t)g.zp + off - (int32_t)kMagicBits;
+        g.lo_ok = g.fast && mn_ok && (int32_t)__float_as_uint(__fadd_rn(a, kMagic)) + g.zoff >= q.qmin + off;
+    } else {
+        g.zp = 0.0f;
+        g.fast = qok;
+        g.zoff = off - (int32_t)kMagicBits;
+        g.lo_ok = qok;
+    }
     return g;
 }
 
 // Eight elements (one uint4 of bf16) -> eight clean codes, fast quotient.
 // kq holds the four pairs' quotient constants; zo[j] the per-element offset.
-template <bool ASYM>
+// LO = false drops the lower clip (valid when every group's lo_ok holds).
+template <bool ASYM, bool LO = true>
 __device__ __forceinline__ void codes8_fast(const uint4& w, const QuotK (&kq)[4], const int32_t (&zo)[8],
                                             int lo_c, int hi_c, uint32_t (&c)[8]) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const u64 r = rint_bits2(quot2(widen_bf16x2(ws[j]), kq[j]));
-        if (ASYM) {
+        if (ASYM && LO) {
             c[2 * j] = (uint32_t)min(__viaddmax_s32((int)lo_bits(r), zo[2 * j], lo_c), hi_c);
             c[2 * j + 1] = (uint32_t)min(__viaddmax_s32((int)hi_bits(r), zo[2 * j + 1], lo_c), hi_c);
+        } else if (ASYM) {
+            c[2 * j] = (uint32_t)__viaddmin_s32((int)lo_bits(r), zo[2 * j], hi_c);
+            c[2 * j + 1] = (uint32_t)__viaddmin_s32((int)hi_bits(r), zo[2 * j + 1], hi_c);
         } else {
             c[2 * j] = lo_bits(r) + (uint32_t)zo[2 * j];
             c[2 * j + 1] = hi_bits(r) + (uint32_t)zo[2 * j + 1];

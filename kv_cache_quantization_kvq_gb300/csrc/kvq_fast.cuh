@@ -7,13 +7,15 @@
 //    instruction rounds two independent float32 results exactly as two
 //    scalar instructions would;
 //  * x / s is the exact IEEE quotient computed from the group's reciprocal
-//    inv = RN(1/s) with FMA remainder corrections (Markstein's division
-//    method: q = RN(x*inv); r = x - s*q is exact in one FMA; q += r*inv),
-//    so no per-element reciprocal instruction is issued.  A unit test checks
-//    it bit for bit against __fdiv_rn exhaustively over bf16 operands when
+//    inv = RN(1/s) with one FMA remainder correction (Markstein's division
+//    theorem: with q = RN(x*inv), the remainder r = x - s*q is exact in one
+//    FMA and RN(q + r*inv) is the correctly rounded quotient), so no
+//    per-element reciprocal instruction is issued.  A unit test checks it
+//    bit for bit against __fdiv_rn exhaustively over bf16 operands when
 //    |x| and |x / s| are at least 2^-100; below that the remainder or the
 //    quotient underflows, but then |x / s| is far below 1/2 and the rounded
 //    code -- the only thing used -- is the same (also checked exhaustively);
+//    the same method divides a group's range by the integer qmax - qmin;
 //  * round-to-nearest-even to an integer is one add of 1.5*2^23: for
 //    |y| < 2^22 the sum is exact and its bit pattern is 0x4B400000 + rint(y),
 //    so the integer code is read from the bits with no conversion
@@ -89,21 +91,17 @@ __device__ __forceinline__ QuotK quot_consts(float s_lo, float s_hi) {
     return k;
 }
 
-// RN(x / s) for both lanes of a pair (Markstein: two remainder corrections).
+// RN(x / s) for both lanes of a pair (one Markstein remainder correction).
 __device__ __forceinline__ u64 quot2(u64 x, const QuotK& k) {
-    u64 q = mul2(x, k.inv);
-    u64 r = fma2(k.ns, q, x);
-    q = fma2(r, k.inv, q);
-    r = fma2(k.ns, q, x);
+    const u64 q = mul2(x, k.inv);
+    const u64 r = fma2(k.ns, q, x);
     return fma2(r, k.inv, q);
 }
 
 // scalar version (per-group bookkeeping)
 __device__ __forceinline__ float quot1(float x, float s, float inv) {
-    float q = __fmul_rn(x, inv);
-    float r = __fmaf_rn(-s, q, x);
-    q = __fmaf_rn(r, inv, q);
-    r = __fmaf_rn(-s, q, x);
+    const float q = __fmul_rn(x, inv);
+    const float r = __fmaf_rn(-s, q, x);
     return __fmaf_rn(r, inv, q);
 }
 

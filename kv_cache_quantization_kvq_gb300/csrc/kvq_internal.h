@@ -22,6 +22,7 @@ struct QSpec {
     int32_t is_signed;                      // codes are two's complement
     int32_t aligned;                        // all buffers 16-byte aligned
     float lo, hi;                           // clip range as floats
+    float inv_qr;                           // RN(1 / (qmax - qmin)) (asym) or RN(1 / qmax) (sym); 0: not used
 };
 
 struct QArgs {

@@ -19,6 +19,7 @@
 // source load and output store is coalesced; group constants are loaded once
 // per lane item.
 #include <algorithm>
+#include <type_traits>
 
 #include "kvq_bulk.cuh"
 #include "kvq_elem.cuh"
@@ -386,7 +387,7 @@ wq_t_kernel(const QArgs a)
             const uint32_t wmx[2] = {h ? mx[2] : mx[0], h ? mx[3] : mx[1]};
             float os[4], oi[4], oz[4];
             int32_t ozo[4];
-            bool fast = true;
+            bool fast = true, lo_ok = true;
             const int64_t mi = ((int64_t)o * ng + k) * C + c8 * 8 + 4 * h;
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
@@ -397,8 +398,10 @@ wq_t_kernel(const QArgs a)
                 write_meta_t<SDT, ZDT>(a, mi + jj, gc);
                 os[jj] = gc.s; oi[jj] = gc.inv; oz[jj] = gc.zp; ozo[jj] = gc.zoff;
                 fast = fast && gc.fast;
+                lo_ok = lo_ok && gc.lo_ok;
             }
             const bool all_fast = __all_sync(0xFFFFFFFFu, fast);
+            const bool no_lo_clip = __all_sync(0xFFFFFFFFu, lo_ok);
             // the partner half's four channels
             float ps[4], pi[4];
             int32_t pzo[4];
@@ -424,17 +427,18 @@ wq_t_kernel(const QArgs a)
                     kq[p].ns = pk(-s8[2 * p], -s8[2 * p + 1]);
                     kq[p].inv = pk(i8[2 * p], i8[2 * p + 1]);
                 }
-                auto emit = [&](int i) {
+                auto emit = [&](int i, auto lo_clip) {
                     uint32_t cc[8];
-                    codes8_fast<ASYM>(*reinterpret_cast<const uint4*>(tile + i * 2 * kRowB), kq, zo, lo_c, hi_c, cc);
+                    codes8_fast<ASYM, decltype(lo_clip)::value>(*reinterpret_cast<const uint4*>(tile + i * 2 * kRowB),
+                                                                kq, zo, lo_c, hi_c, cc);
                     store_codes<BITS>(cp + (uint64_t)i * 2 * kCodeRowB, finish_word<BITS>(cc, q.is_signed));
                 };
-                if (whole) {
+                if (whole && (!ASYM || no_lo_clip)) {
 #pragma unroll 4
-                    for (int i = 0; i < RPL; ++i) emit(i);
+                    for (int i = 0; i < RPL; ++i) emit(i, std::false_type{});
                 } else {
                     for (int i = 0; i < RPL; ++i)
-                        if (2 * i + h < nrows) emit(i);
+                        if (2 * i + h < nrows) emit(i, std::true_type{});
                 }
             } else {
                 float pz[4], z8[8];
@@ -536,11 +540,20 @@ sq_c_kernel(const QArgs a)
                 int32_t zo[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) zo[j] = gc.zoff;
+                if (gc.lo_ok) {
 #pragma unroll
-                for (int k = 0; k < WPG; ++k) {
-                    uint32_t cc[8];
-                    codes8_fast<ASYM>(w[gg * WPG + k], kq, zo, lo_c, hi_c, cc);
-                    cw[gg * WPG + k] = finish_word<BITS>(cc, q.is_signed);
+                    for (int k = 0; k < WPG; ++k) {
+                        uint32_t cc[8];
+                        codes8_fast<ASYM, false>(w[gg * WPG + k], kq, zo, lo_c, hi_c, cc);
+                        cw[gg * WPG + k] = finish_word<BITS>(cc, q.is_signed);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < WPG; ++k) {
+                        uint32_t cc[8];
+                        codes8_fast<ASYM>(w[gg * WPG + k], kq, zo, lo_c, hi_c, cc);
+                        cw[gg * WPG + k] = finish_word<BITS>(cc, q.is_signed);
+                    }
                 }
             } else {
                 float s8[8], z8[8];

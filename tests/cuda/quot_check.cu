@@ -1,12 +1,14 @@
 // Exhaustive check of the fast-path arithmetic in kvq_fast.cuh against CUDA's
 // IEEE operations:
-//  1. quot1 / quot2 (reciprocal + two FMA remainder corrections) == __fdiv_rn
+//  1. quot1 / quot2 (reciprocal + one FMA remainder correction) == __fdiv_rn
 //     bit for bit for every bf16 x and bf16 scale s (|x|, |x/s| >= 2^-100)
 //     inside the fast domain, and the rounded codes agree for every x;
 //  2. the same for every bf16 x and the float32 scales RN(a / qmax) of every
 //     bf16 abs-max a and every qmax used by the formats (1, 3, 7, 15, 127, 255);
 //  3. 2^30 random float32 pairs (counter-based hash) inside the fast domain;
-//  4. bits(y + 1.5*2^23) - 0x4B400000 == rintf(y) for every float |y| < 2^21.
+//  4. bits(y + 1.5*2^23) - 0x4B400000 == rintf(y) for every float |y| < 2^21;
+//  5. the group-range division: quot1(r, n, RN(1/n)) == __fdiv_rn(r, n) for
+//     every float r in [2^-100, 2^127] and every integer n in 1..255.
 // Prints the mismatch counts; exit status 0 only if all are zero.
 #include <cstdio>
 #include <cstdint>
@@ -14,10 +16,10 @@
 
 using namespace kvq;
 
-__device__ unsigned long long g_bad[4];
+__device__ unsigned long long g_bad[5];
 __device__ unsigned int g_nex;
 __device__ float g_ex[64][5];   // first failing pairs: x, s, quotient, __fdiv_rn, slot
-__device__ unsigned long long g_checked[4];
+__device__ unsigned long long g_checked[5];
 
 __device__ __forceinline__ bool bf16_finite(uint32_t b) { return ((b >> 7) & 0xFF) != 0xFF; }
 
@@ -115,8 +117,26 @@ __global__ void magic_round() {
     atomicAdd(&g_checked[3], n);
 }
 
+// 5. range / integer divisor, every float r in [2^-100, 2^127], divisor n
+__global__ void range_div(float n) {
+    unsigned long long bad = 0, cnt = 0;
+    const float inv = __frcp_rn(n);
+    const uint32_t lo = 0x0D800000u, hi = 0x7F000000u;   // 2^-100 .. 2^127
+    for (uint64_t i = lo + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i <= hi; i += (uint64_t)gridDim.x * blockDim.x) {
+        const float r = __uint_as_float((uint32_t)i);
+        ++cnt;
+        if (__float_as_uint(quot1(r, n, inv)) != __float_as_uint(__fdiv_rn(r, n))) {
+            ++bad;
+            const unsigned int e = atomicAdd(&g_nex, 1u);
+            if (e < 64) { g_ex[e][0] = r; g_ex[e][1] = n; g_ex[e][2] = quot1(r, n, inv); g_ex[e][3] = __fdiv_rn(r, n); g_ex[e][4] = 5.0f; }
+        }
+    }
+    atomicAdd(&g_bad[4], bad);
+    atomicAdd(&g_checked[4], cnt);
+}
+
 int main() {
-    const unsigned long long zero[4] = {0, 0, 0, 0};
+    const unsigned long long zero[5] = {0, 0, 0, 0, 0};
     cudaMemcpyToSymbol(g_bad, zero, sizeof(zero));
     cudaMemcpyToSymbol(g_checked, zero, sizeof(zero));
     const unsigned int z0 = 0;
@@ -129,12 +149,14 @@ int main() {
     for (float qm : qmaxes) bf16_x_f32_scales<<<grid, block>>>(qm);
     f32_random<<<grid, block>>>();
     magic_round<<<grid, block>>>();
+    for (int n = 1; n <= 255; ++n) range_div<<<grid, block>>>((float)n);
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) { printf("CUDA error: %s\n", cudaGetErrorString(e)); return 2; }
-    unsigned long long bad[4], n[4];
+    unsigned long long bad[5], n[5];
     cudaMemcpyFromSymbol(bad, g_bad, sizeof(bad));
     cudaMemcpyFromSymbol(n, g_checked, sizeof(n));
-    const char* names[4] = {"bf16 x / bf16 s", "bf16 x / f32 RN(a/qmax)", "random f32 pairs", "magic rint |y|<2^21"};
+    const char* names[5] = {"bf16 x / bf16 s", "bf16 x / f32 RN(a/qmax)", "random f32 pairs", "magic rint |y|<2^21",
+                            "range / n, n = 1..255"};
     unsigned int nex = 0;
     float ex[64][5];
     cudaMemcpyFromSymbol(&nex, g_nex, sizeof(nex));
@@ -142,7 +164,7 @@ int main() {
     for (unsigned int i = 0; i < nex && i < 64; ++i)
         printf("mismatch slot %d: x=%a s=%a quotient=%a fdiv=%a\n", (int)ex[i][4], ex[i][0], ex[i][1], ex[i][2], ex[i][3]);
     int rc = 0;
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 5; ++i) {
         printf("%-26s checked %llu mismatches %llu\n", names[i], n[i], bad[i]);
         if (bad[i] || !n[i]) rc = 1;
     }

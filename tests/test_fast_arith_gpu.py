@@ -1,9 +1,11 @@
 """Bit-exactness of the fast paths' arithmetic against CUDA's own IEEE
-operations: the reciprocal-plus-remainder-correction quotient equals
+operations: the reciprocal-plus-one-remainder-correction quotient equals
 __fdiv_rn for every bf16 operand pair (and for float32 scales RN(a/qmax) of
 every bf16 abs-max, and 2^30 random float32 pairs) inside its domain when
-|x| and |x/s| are at least 2^-100, the rounded integer codes agree for every pair, and the
-1.5*2^23 rounding trick equals rintf for every float of magnitude < 2^21."""
+|x| and |x/s| are at least 2^-100, the rounded integer codes agree for every
+pair, the 1.5*2^23 rounding trick equals rintf for every float of magnitude
+< 2^21, and a group range divided by any integer 1..255 this way equals
+__fdiv_rn for every float in [2^-100, 2^127]."""
 import os
 import subprocess
 
