@@ -21,6 +21,8 @@
 #include <algorithm>
 #include <type_traits>
 
+#include <cudaTypedefs.h>
+
 #include "kvq_bulk.cuh"
 #include "kvq_elem.cuh"
 
@@ -263,15 +265,19 @@ sq_t_kernel(const QArgs a)
 // ======================================================================
 // groups along T, warp-specialised (C = 128, g in {16, 32, 64}).  A producer
 // warp keeps a ring of kWStages stages full with bulk copies; each stage is
-// one group tile [g tokens x 128 channels] and belongs to one consumer warp
-// for the whole of its processing: lane = 8 channels x every other token of
-// the tile, so a group's min / max is one shuffle away and no block-wide
+// one group tile [g tokens x 128 channels] and is consumed by one pair of
+// warps, one per 64-channel half: lane = 8 channels x every fourth token of
+// the tile, so a group's min / max is two shuffles away and no block-wide
 // barrier is ever taken.  Stage s is handed back to the producer by one
-// arrival on empty[s].
+// arrival of each warp of the pair on empty[s].  Stage s belongs to pair
+// s % kWPairs (kWStages is a multiple of kWPairs): when a pair waits for the
+// phase of chunk j on its stage it has itself consumed chunk j - kWStages
+// there, so the phase parity it waits on cannot be confused with an older one.
 // ======================================================================
-constexpr int kWConsumers = 8;
-constexpr int kWStages = 13;
-constexpr int kWThreads = (kWConsumers + 1) * 32;
+constexpr int kWPairs = 6;
+constexpr int kWStages = 12;
+static_assert(kWStages % kWPairs == 0, "a stage must belong to one consumer pair");
+constexpr int kWThreads = (2 * kWPairs + 1) * 32;
 constexpr int kWSmem = kWStages * kStageBytes + 2 * kWStages * 8;
 
 template <int BITS, bool ASYM, int G, int SDT, int ZDT>
@@ -279,7 +285,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
 wq_t_kernel(const QArgs a)
 {
     constexpr int C = 128;
-    constexpr int RPL = G / 2;                          // rows per lane in a full tile
+    constexpr int RPL = G / 4;                          // rows per lane in a full tile
     constexpr uint32_t kRowB = C * 2;                   // bytes of one bf16 row
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWStages * kStageBytes);
@@ -297,7 +303,7 @@ wq_t_kernel(const QArgs a)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kWStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);
         }
         mbar_init_fence();
     }
@@ -313,7 +319,7 @@ wq_t_kernel(const QArgs a)
     };
     const uint32_t first = blockIdx.x, step = gridDim.x;
 
-    if (warp == kWConsumers) {
+    if (warp == 2 * kWPairs) {
         // ---- producer: one lane issues every copy of this CTA
         if (lane != 0) return;
         uint32_t n = 0;
@@ -334,30 +340,32 @@ wq_t_kernel(const QArgs a)
         return;
     }
 
-    // ---- consumers
-    const int c8 = lane & 15, h = lane >> 4;
+    // ---- consumers: warp pair p, channel half e
+    const int pair = warp >> 1, e = warp & 1;
+    const int c8 = lane & 7, rq = lane >> 3;            // 8 channels x rows rq, rq+4, ...
     const int off = q.is_signed ? (1 << (BITS - 1)) : 0;
     const int lo_c = q.qmin + off, hi_c = q.qmax + off;
     uint8_t* codes = static_cast<uint8_t*>(a.codes);
     constexpr uint32_t kCodeRowB = C * BITS / 8;
-    for (uint32_t j = warp;; j += kWConsumers) {
+    const int chan0 = e * 64 + c8 * 8;                   // first of this lane's 8 channels
+    for (uint32_t j = pair;; j += kWPairs) {
         const uint32_t c = first + j * step;
         if (c >= nchunks) break;
         const int s = (int)(j % kWStages);
-        if (!mbar_wait(&full[s], (j / kWStages) & 1u)) return;   // recorded in g_kvq_wait_timeouts
-        const unsigned char* tile = smem + s * kStageBytes + c8 * 16 + h * kRowB;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (j / kWStages) & 1u))) return;   // recorded in g_kvq_wait_timeouts
+        const unsigned char* tile = smem + s * kStageBytes + chan0 * 2 + rq * kRowB;
         uint32_t o, k, row0; int nrows; bool res;
         geom(c, o, k, row0, nrows, res);
         const bool whole = nrows == G;
         if (res) {
             __nv_bfloat16* rp = static_cast<__nv_bfloat16*>(a.resid) +
-                                (((uint64_t)o * q.R + (row0 - Tq32) + h) * C + c8 * 8);
+                                (((uint64_t)o * q.R + (row0 - Tq32) + rq) * C + chan0);
 #pragma unroll 4
             for (int i = 0; i < RPL; ++i)
-                if (2 * i + h < nrows)
-                    *reinterpret_cast<uint4*>(rp + (uint64_t)i * 2 * C) = *reinterpret_cast<const uint4*>(tile + i * 2 * kRowB);
+                if (4 * i + rq < nrows)
+                    *reinterpret_cast<uint4*>(rp + (uint64_t)i * 4 * C) = *reinterpret_cast<const uint4*>(tile + i * 4 * kRowB);
         } else {
-            // group min / max (abs-max when symmetric) over the lane's rows, then over both halves
+            // group min / max (abs-max when symmetric) over the lane's rows, then over the 4 row slices
             uint32_t mn[4], mx[4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) { mn[p] = kBfPosInf2; mx[p] = ASYM ? kBfNegInf2 : 0u; }
@@ -371,55 +379,44 @@ wq_t_kernel(const QArgs a)
             };
             if (whole) {
 #pragma unroll 8
-                for (int i = 0; i < RPL; ++i) fold(*reinterpret_cast<const uint4*>(tile + i * 2 * kRowB));
+                for (int i = 0; i < RPL; ++i) fold(*reinterpret_cast<const uint4*>(tile + i * 4 * kRowB));
             } else {
 #pragma unroll 4
                 for (int i = 0; i < RPL; ++i)
-                    if (2 * i + h < nrows) fold(*reinterpret_cast<const uint4*>(tile + i * 2 * kRowB));
+                    if (4 * i + rq < nrows) fold(*reinterpret_cast<const uint4*>(tile + i * 4 * kRowB));
             }
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                if (ASYM) mn[p] = bmin2(mn[p], __shfl_xor_sync(0xFFFFFFFFu, mn[p], 16));
-                mx[p] = bmax2(mx[p], __shfl_xor_sync(0xFFFFFFFFu, mx[p], 16));
-            }
-            // lane half h derives the constants of channels 4h .. 4h+3 of its 8
-            const uint32_t wmn[2] = {h ? mn[2] : mn[0], h ? mn[3] : mn[1]};
-            const uint32_t wmx[2] = {h ? mx[2] : mx[0], h ? mx[3] : mx[1]};
-            float os[4], oi[4], oz[4];
-            int32_t ozo[4];
-            bool fast = true, lo_ok = true;
-            const int64_t mi = ((int64_t)o * ng + k) * C + c8 * 8 + 4 * h;
+            for (int sft = 8; sft < 32; sft <<= 1) {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const uint32_t m0 = wmn[jj >> 1], m1 = wmx[jj >> 1];
-                const float fmn = (jj & 1) ? hi_f(m0) : lo_f(m0);
-                const float fmx = (jj & 1) ? hi_f(m1) : lo_f(m1);
-                const GroupC gc = make_group<ASYM>(fmn, fmx, q, off);
-                write_meta_t<SDT, ZDT>(a, mi + jj, gc);
-                os[jj] = gc.s; oi[jj] = gc.inv; oz[jj] = gc.zp; ozo[jj] = gc.zoff;
-                fast = fast && gc.fast;
-                lo_ok = lo_ok && gc.lo_ok;
+                for (int p = 0; p < 4; ++p) {
+                    if (ASYM) mn[p] = bmin2(mn[p], __shfl_xor_sync(0xFFFFFFFFu, mn[p], sft));
+                    mx[p] = bmax2(mx[p], __shfl_xor_sync(0xFFFFFFFFu, mx[p], sft));
+                }
             }
-            const bool all_fast = __all_sync(0xFFFFFFFFu, fast);
-            const bool no_lo_clip = __all_sync(0xFFFFFFFFu, lo_ok);
-            // the partner half's four channels
-            float ps[4], pi[4];
-            int32_t pzo[4];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                ps[jj] = __shfl_xor_sync(0xFFFFFFFFu, os[jj], 16);
-                pi[jj] = __shfl_xor_sync(0xFFFFFFFFu, oi[jj], 16);
-                pzo[jj] = __shfl_xor_sync(0xFFFFFFFFu, ozo[jj], 16);
-            }
+            // row slice rq derives the constants of channel pair rq (channels 2rq, 2rq+1)
+            const uint32_t wmn = rq == 0 ? mn[0] : rq == 1 ? mn[1] : rq == 2 ? mn[2] : mn[3];
+            const uint32_t wmx = rq == 0 ? mx[0] : rq == 1 ? mx[1] : rq == 2 ? mx[2] : mx[3];
+            const int64_t mi = ((int64_t)o * ng + k) * C + chan0 + 2 * rq;
+            const GroupC g0 = make_group<ASYM>(lo_f(wmn), lo_f(wmx), q, off);
+            const GroupC g1 = make_group<ASYM>(hi_f(wmn), hi_f(wmx), q, off);
+            write_meta_t<SDT, ZDT>(a, mi, g0);
+            write_meta_t<SDT, ZDT>(a, mi + 1, g1);
+            const bool all_fast = __all_sync(0xFFFFFFFFu, g0.fast && g1.fast);
+            const bool no_lo_clip = __all_sync(0xFFFFFFFFu, g0.lo_ok && g1.lo_ok);
+            // every lane gathers the constants of its four channel pairs from row slices 0..3
             float s8[8], i8[8];
             int32_t zo[8];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                s8[jj] = h ? ps[jj] : os[jj];       s8[jj + 4] = h ? os[jj] : ps[jj];
-                i8[jj] = h ? pi[jj] : oi[jj];       i8[jj + 4] = h ? oi[jj] : pi[jj];
-                zo[jj] = h ? pzo[jj] : ozo[jj];     zo[jj + 4] = h ? ozo[jj] : pzo[jj];
+            for (int p = 0; p < 4; ++p) {
+                const int src = c8 + 8 * p;
+                s8[2 * p] = __shfl_sync(0xFFFFFFFFu, g0.s, src);
+                s8[2 * p + 1] = __shfl_sync(0xFFFFFFFFu, g1.s, src);
+                i8[2 * p] = __shfl_sync(0xFFFFFFFFu, g0.inv, src);
+                i8[2 * p + 1] = __shfl_sync(0xFFFFFFFFu, g1.inv, src);
+                zo[2 * p] = __shfl_sync(0xFFFFFFFFu, g0.zoff, src);
+                zo[2 * p + 1] = __shfl_sync(0xFFFFFFFFu, g1.zoff, src);
             }
-            uint8_t* cp = codes + ((uint64_t)o * Tq32 + row0 + h) * kCodeRowB + (uint32_t)c8 * BITS;
+            uint8_t* cp = codes + ((uint64_t)o * Tq32 + row0 + rq) * kCodeRowB + (uint32_t)(chan0 / 8) * BITS;
             if (all_fast) {
                 QuotK kq[4];
 #pragma unroll
@@ -429,29 +426,198 @@ wq_t_kernel(const QArgs a)
                 }
                 auto emit = [&](int i, auto lo_clip) {
                     uint32_t cc[8];
-                    codes8_fast<ASYM, decltype(lo_clip)::value>(*reinterpret_cast<const uint4*>(tile + i * 2 * kRowB),
+                    codes8_fast<ASYM, decltype(lo_clip)::value>(*reinterpret_cast<const uint4*>(tile + i * 4 * kRowB),
                                                                 kq, zo, lo_c, hi_c, cc);
-                    store_codes<BITS>(cp + (uint64_t)i * 2 * kCodeRowB, finish_word<BITS>(cc, q.is_signed));
+                    store_codes<BITS>(cp + (uint64_t)i * 4 * kCodeRowB, finish_word<BITS>(cc, q.is_signed));
                 };
                 if (whole && (!ASYM || no_lo_clip)) {
 #pragma unroll 4
                     for (int i = 0; i < RPL; ++i) emit(i, std::false_type{});
                 } else {
                     for (int i = 0; i < RPL; ++i)
-                        if (2 * i + h < nrows) emit(i, std::true_type{});
+                        if (4 * i + rq < nrows) emit(i, std::true_type{});
                 }
             } else {
-                float pz[4], z8[8];
+                float z8[8];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) pz[jj] = __shfl_xor_sync(0xFFFFFFFFu, oz[jj], 16);
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) { z8[jj] = h ? pz[jj] : oz[jj]; z8[jj + 4] = h ? oz[jj] : pz[jj]; }
+                for (int p = 0; p < 4; ++p) {
+                    const int src = c8 + 8 * p;
+                    z8[2 * p] = __shfl_sync(0xFFFFFFFFu, g0.zp, src);
+                    z8[2 * p + 1] = __shfl_sync(0xFFFFFFFFu, g1.zp, src);
+                }
                 for (int i = 0; i < RPL; ++i)
-                    if (2 * i + h < nrows) {
+                    if (4 * i + rq < nrows) {
                         uint32_t cc[8];
-                        codes8_slow<ASYM>(*reinterpret_cast<const uint4*>(tile + i * 2 * kRowB), s8, z8, q, off, cc);
-                        store_codes<BITS>(cp + (uint64_t)i * 2 * kCodeRowB, finish_word<BITS>(cc, q.is_signed));
+                        codes8_slow<ASYM>(*reinterpret_cast<const uint4*>(tile + i * 4 * kRowB), s8, z8, q, off, cc);
+                        store_codes<BITS>(cp + (uint64_t)i * 4 * kCodeRowB, finish_word<BITS>(cc, q.is_signed));
                     }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+// ======================================================================
+// groups along C, warp-specialised (C = 128, g in {32, 64, 128}).  A chunk is
+// 32 consecutive token rows, brought in by two 2-D TMA loads (channels 0-63
+// and 64-127, 4 KB each) with the 128-byte swizzle: within each 1 KB block the
+// 16-byte column u of row r lands at slot u ^ (r & 7), so lane l reading
+// column u of row l hits a different bank group than lanes l+1 .. l+7.  Each
+// of the kCConsumers consumer warps owns whole chunks: lane = one token row,
+// so a group's reduction and constants stay in one thread.
+// ======================================================================
+constexpr int kCConsumers = 12;
+constexpr int kCRows = 32;
+constexpr int kCHalfB = kCRows * 128;                      // one 64-channel box
+constexpr int kCStageB = 2 * kCHalfB;                      // 8192
+constexpr int kCStages = 24;
+static_assert(kCStages % kCConsumers == 0, "a stage must belong to one consumer warp");
+constexpr int kCThreads = (kCConsumers + 1) * 32;
+constexpr int kCSmem = 1024 + kCStages * kCStageB + 2 * kCStages * 8;   // + alignment slack
+
+template <int BITS, bool ASYM, int G, int SDT, int ZDT>
+__global__ void __launch_bounds__(kCThreads, 1)
+wq_c_kernel(const QArgs a, const __grid_constant__ CUtensorMap tmap)
+{
+    constexpr int C = 128;
+    constexpr int GPR = C / G;                 // groups per row
+    constexpr int WPG = G / 8;                 // 16-byte words per group
+    using W = typename CodeWord<BITS>::T;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    // the swizzled boxes need 1 KB alignment
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kCStages * kCStageB);
+    uint64_t* empty = full + kCStages;
+
+    const QSpec& q = a.q;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t T32 = (uint32_t)q.T, Tq32 = (uint32_t)q.Tq;
+    const uint32_t nrows_total = (uint32_t)(q.outer * q.T);       // < 2^31, checked by the dispatcher
+    const uint32_t nchunks = (nrows_total + kCRows - 1) / kCRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kCStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const uint32_t first = blockIdx.x, step = gridDim.x;
+
+    if (warp == kCConsumers) {
+        // ---- producer: one lane issues both boxes of every chunk of this CTA
+        if (lane != 0) return;
+        uint32_t n = 0;
+        for (;; ++n) {
+            const uint32_t c = first + n * step;
+            if (c >= nchunks) break;
+            const int s = (int)(n % kCStages);
+            if (n >= (uint32_t)kCStages && !mbar_wait(&empty[s], ((n / kCStages) - 1) & 1u)) break;
+            // rows past the end are zero-filled and still counted in the box bytes
+            mbar_expect_tx(&full[s], (uint32_t)kCStageB);
+            tma_load_2d(smem + s * kCStageB, &tmap, 0, (int)(c * kCRows), &full[s]);
+            tma_load_2d(smem + s * kCStageB + kCHalfB, &tmap, 64, (int)(c * kCRows), &full[s]);
+        }
+        for (uint32_t i = n > (uint32_t)kCStages ? n - kCStages : 0; i < n; ++i)
+            mbar_wait(&full[i % kCStages], (i / kCStages) & 1u);
+        return;
+    }
+
+    // ---- consumers
+    const int off = q.is_signed ? (1 << (BITS - 1)) : 0;
+    const int lo_c = q.qmin + off, hi_c = q.qmax + off;
+    uint8_t* codes = static_cast<uint8_t*>(a.codes);
+    constexpr uint32_t kCodeRowB = C * BITS / 8;
+    for (uint32_t j = warp;; j += kCConsumers) {
+        const uint32_t c = first + j * step;
+        if (c >= nchunks) break;
+        const int s = (int)(j % kCStages);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (j / kCStages) & 1u))) return;   // recorded in g_kvq_wait_timeouts
+        const uint32_t row = c * kCRows + lane;
+        const unsigned char* rp = smem + s * kCStageB + lane * 128;
+        const int sw = lane & 7;
+        // 16-byte column k (0..15) of this lane's row
+        auto word = [&](int k) -> uint4 {
+            return *reinterpret_cast<const uint4*>(rp + (k >> 3) * kCHalfB + (((k & 7) ^ sw) << 4));
+        };
+        if (row < nrows_total) {
+            const uint32_t o = row / T32, t = row - o * T32;
+            if (t >= Tq32) {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.resid) +
+                                                      ((uint64_t)o * q.R + (t - Tq32)) * C);
+#pragma unroll
+                for (int k = 0; k < C / 8; ++k) dst[k] = word(k);
+            } else {
+                const uint64_t qrow = (uint64_t)o * Tq32 + t;
+                W cw[C / 8];
+#pragma unroll
+                for (int gi = 0; gi < GPR; ++gi) {
+                    uint32_t mn = kBfPosInf2, mx = ASYM ? kBfNegInf2 : 0u;
+#pragma unroll
+                    for (int k = 0; k < WPG; ++k) {
+                        const uint4 w = word(gi * WPG + k);
+                        if (ASYM) fold_minmax(w, mn, mx);
+                        else fold_absmax(w, mx);
+                    }
+                    const GroupC gc = make_group<ASYM>(fminf(lo_f(mn), hi_f(mn)), fmaxf(lo_f(mx), hi_f(mx)), q, off);
+                    write_meta_t<SDT, ZDT>(a, (int64_t)qrow * GPR + gi, gc);
+                    if (gc.fast) {
+                        QuotK kq[4];
+                        kq[0].ns = pk(-gc.s, -gc.s);
+                        kq[0].inv = pk(gc.inv, gc.inv);
+                        kq[1] = kq[2] = kq[3] = kq[0];
+                        int32_t zo[8];
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) zo[jj] = gc.zoff;
+                        if (!ASYM || gc.lo_ok) {
+#pragma unroll
+                            for (int k = 0; k < WPG; ++k) {
+                                uint32_t cc[8];
+                                codes8_fast<ASYM, false>(word(gi * WPG + k), kq, zo,
+                                                         lo_c, hi_c, cc);
+                                cw[gi * WPG + k] = finish_word<BITS>(cc, q.is_signed);
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < WPG; ++k) {
+                                uint32_t cc[8];
+                                codes8_fast<ASYM>(word(gi * WPG + k), kq, zo,
+                                                  lo_c, hi_c, cc);
+                                cw[gi * WPG + k] = finish_word<BITS>(cc, q.is_signed);
+                            }
+                        }
+                    } else {
+                        float s8[8], z8[8];
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) { s8[jj] = gc.s; z8[jj] = gc.zp; }
+#pragma unroll
+                        for (int k = 0; k < WPG; ++k) {
+                            uint32_t cc[8];
+                            codes8_slow<ASYM>(word(gi * WPG + k), s8, z8, q, off, cc);
+                            cw[gi * WPG + k] = finish_word<BITS>(cc, q.is_signed);
+                        }
+                    }
+                }
+                // the row's codes: kCodeRowB bytes, 16-byte stores
+                uint4* cdst = reinterpret_cast<uint4*>(codes + qrow * kCodeRowB);
+                constexpr int WPS = 16 / sizeof(W);          // code words per 16-byte store
+#pragma unroll
+                for (int k = 0; k < (C / 8) / WPS; ++k) {
+                    uint4 v;
+                    if constexpr (BITS == 8) {
+                        v = make_uint4(cw[2 * k].x, cw[2 * k].y, cw[2 * k + 1].x, cw[2 * k + 1].y);
+                    } else if constexpr (BITS == 4) {
+                        v = make_uint4(cw[4 * k], cw[4 * k + 1], cw[4 * k + 2], cw[4 * k + 3]);
+                    } else {
+                        v = make_uint4((uint32_t)cw[8 * k] | ((uint32_t)cw[8 * k + 1] << 16),
+                                       (uint32_t)cw[8 * k + 2] | ((uint32_t)cw[8 * k + 3] << 16),
+                                       (uint32_t)cw[8 * k + 4] | ((uint32_t)cw[8 * k + 5] << 16),
+                                       (uint32_t)cw[8 * k + 6] | ((uint32_t)cw[8 * k + 7] << 16));
+                    }
+                    cdst[k] = v;
+                }
             }
         }
         __syncwarp();
@@ -776,9 +942,61 @@ void sq_t_launch(const QArgs& a, cudaStream_t st) {
     sq_t_kernel<BITS, ASYM, 128, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a);
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &r) != cudaSuccess ||
+            r != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// [rows, 128] bf16 rows of x as boxes of 64 channels x kCRows rows, 128-byte swizzle.
+bool encode_rows_map(const QSpec& q, const void* x, CUtensorMap* map) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)q.C, (cuuint64_t)(q.outer * q.T)};
+    const cuuint64_t strides[1] = {(cuuint64_t)q.C * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kCRows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BITS, bool ASYM, int G, int SDT, int ZDT>
+bool wq_c_launch(const QArgs& a, cudaStream_t st) {
+    const QSpec& q = a.q;
+    CUtensorMap map;
+    if (!encode_rows_map(q, a.x, &map)) return false;
+    const uint64_t nchunks = ((uint64_t)q.outer * q.T + kCRows - 1) / kCRows;
+    const unsigned grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(nchunks, (uint64_t)sm_count()));
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(wq_c_kernel<BITS, ASYM, G, SDT, ZDT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCSmem);
+        attr = true;
+    }
+    wq_c_kernel<BITS, ASYM, G, SDT, ZDT><<<grid, kCThreads, kCSmem, st>>>(a, map);
+    return true;
+}
+
 template <int BITS, bool ASYM, int SDT, int ZDT>
 void sq_c_launch(const QArgs& a, cudaStream_t st) {
     const QSpec& q = a.q;
+    if (q.C == 128) {
+        bool done = false;
+        switch (q.g) {
+        case 32: done = wq_c_launch<BITS, ASYM, 32, SDT, ZDT>(a, st); break;
+        case 64: done = wq_c_launch<BITS, ASYM, 64, SDT, ZDT>(a, st); break;
+        case 128: done = wq_c_launch<BITS, ASYM, 128, SDT, ZDT>(a, st); break;
+        default: break;
+        }
+        if (done) return;
+    }
     const uint64_t rc = kStageBytes / (2 * q.C);
     const uint64_t nchunks = ((uint64_t)q.outer * q.T + rc - 1) / rc;
     const unsigned grid = staged_grid(sm_count(), nchunks);

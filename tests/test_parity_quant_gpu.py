@@ -225,6 +225,44 @@ def test_along_t_head_dim_128_values_and_lengths(b, kind, T, R):
         check_case(b, xin, O.BF16, oq)
 
 
+# head_dim 128 with bf16 input, groups along C: the warp-specialised row
+# kernel (g in {32, 64, 128}) for every metadata layout it specialises, plus
+# g = 16 (the other kernels); token counts that leave a ragged last chunk of
+# 32 rows and chunks that straddle the residual window and the next head.
+HD128_C_CASES = []
+for bits, g in itertools.product((8, 4, 2), (32, 64, 128, 16)):
+    HD128_C_CASES.append(("sym", bits, g, O.BF16, O.NONE, None))
+    HD128_C_CASES.append(("sym", bits, g, O.F32, O.NONE, None))
+    for qr in asym_ranges(bits):
+        HD128_C_CASES.append(("asym", bits, g, O.BF16, O.BF16, qr))
+        HD128_C_CASES.append(("asym", bits, g, O.F32, O.I8, qr))
+
+
+@pytest.mark.parametrize("case", HD128_C_CASES, ids=str)
+def test_along_c_head_dim_128(b, case):
+    mode, bits, g, sdt, zdt, qr = case
+    rng = np.random.default_rng(zlib.crc32(repr(case).encode()))
+    xin = make_input(rng, (3, 301, 128), O.BF16)
+    if mode == "sym":
+        oq = sym(bits, axis=O.ALONG_C, group=g, residual=13, scale_dtype=sdt)
+    else:
+        oq = O.QParams.asym(bits, qr[0], qr[1], axis=O.ALONG_C, group=g, residual=13, scale_dtype=sdt,
+                            zero_dtype=zdt)
+    check_case(b, xin, O.BF16, oq)
+
+
+@pytest.mark.parametrize("kind", ["zeros", "ties", "wide", "const"])
+@pytest.mark.parametrize("T,R", [(200, 0), (45, 64), (33, 1)])
+def test_along_c_head_dim_128_values_and_lengths(b, kind, T, R):
+    rng = np.random.default_rng(T * 11 + R + len(kind))
+    xin = make_input(rng, (2, T, 128), O.BF16, kind)
+    for oq in (O.QParams.asym(4, 0, 15, axis=O.ALONG_C, group=64, residual=R, scale_dtype=O.BF16,
+                              zero_dtype=O.BF16),
+               O.QParams.asym(2, -2, 1, axis=O.ALONG_C, group=32, residual=R, zero_dtype=O.I8),
+               sym(8, axis=O.ALONG_C, group=128, residual=R, scale_dtype=O.BF16)):
+        check_case(b, xin, O.BF16, oq)
+
+
 # ---------------------------------------------------------------- edge cases
 
 
