@@ -144,7 +144,9 @@ KVQ_API kvq_status kvq_dequantize(const void* codes, const void* scale, const vo
 /* RMSE, max |x - x_hat| and mean |x - x_hat| over all N = outer*T*C elements
  * ([FtC] §1.3), x_hat being what kvq_dequantize returns in x_dtype (residual
  * tokens contribute zero error).  x_hat never goes to memory.  out_dev is a
- * device pointer to one kvq_err.  N = 0 is KVQ_EINVAL. */
+ * device pointer to one kvq_err.  N = 0 is KVQ_EINVAL.  The workspace needs
+ * no initialisation: the call zeroes the part of it that must start at zero.
+ * The sums are combined in a fixed order, so equal inputs give equal bits. */
 KVQ_API kvq_status kvq_error_stats(const void* x, kvq_dtype x_dtype, const void* codes, const void* scale,
                            const void* zero, const void* resid, const kvq_shape* shape,
                            const kvq_qparams* p, kvq_err* out_dev,

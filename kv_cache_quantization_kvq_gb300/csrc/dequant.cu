@@ -402,11 +402,16 @@ __global__ void copy_back_residual_kernel(const QArgs a, int64_t n, int es)
 // query (the launch uses the real count, which only lowers the block count).
 constexpr int kMaxSms = 1024;
 
+// Statistics workspace: a 256-byte header (the completion counter of the
+// fused final reduction) followed by one Partial per block.
+constexpr size_t kStatsHeader = 256;
+
 size_t errstats_workspace(const QSpec& q)
 {
     const Geometry G = geometry(q, kMaxSms);
     const int64_t fast = fast_stats_blocks(q, kMaxSms);
-    return std::max<size_t>((size_t)G.grid.x * G.grid.y, (size_t)std::max<int64_t>(fast, 0)) * sizeof(Partial);
+    return kStatsHeader +
+           std::max<size_t>((size_t)G.grid.x * G.grid.y, (size_t)std::max<int64_t>(fast, 0)) * sizeof(Partial);
 }
 
 cudaError_t launch_dequantize(const QArgs& a, int out_dt, cudaStream_t st)
@@ -430,8 +435,15 @@ cudaError_t launch_error_stats(const QArgs& a, kvq_err* out_dev, cudaStream_t st
 {
     const QSpec& q = a.q;
     const Geometry G = geometry(q, sm_count());
-    Partial* partials = static_cast<Partial*>(a.ws);
+    unsigned int* done = static_cast<unsigned int*>(a.ws);
+    Partial* partials = reinterpret_cast<Partial*>(static_cast<char*>(a.ws) + kStatsHeader);
     int64_t nblocks = (int64_t)G.grid.x * G.grid.y;
+    if (q.Tq > 0 && stream_stats_blocks(q, sm_count()) > 0) {
+        // streaming kernel with the final reduction fused into its last block
+        cudaError_t e = cudaMemsetAsync(done, 0, sizeof(unsigned int), st);
+        if (e != cudaSuccess) return e;
+        return stream_error_stats(a, partials, done, out_dev, st);
+    }
     const int64_t fast_blocks = fast_stats_blocks(q, sm_count());
     if (q.Tq > 0 && fast_blocks > 0) {
         nblocks = fast_blocks;

@@ -824,7 +824,7 @@ int64_t fast_stats_blocks(const QSpec& q, int sms)
 
 cudaError_t fast_error_stats(const QArgs& a, void* partials, cudaStream_t st)
 {
-    if (stream_stats_blocks(a.q, 1) > 0) return stream_error_stats(a, partials, st);
+    if (stream_stats_blocks(a.q, 1) > 0) return stream_error_stats(a, partials, nullptr, nullptr, st);
     const DGeo G = dgeo(a.q, sm_count());
     dq_dispatch<true>(a, G, static_cast<Partial*>(partials), st);
     return cudaGetLastError();

@@ -65,7 +65,9 @@ bool staged_quantize(const QArgs& a, cudaStream_t st);          // false: not ha
 bool stream_dequant_supported(const QSpec& q, int out_dt);
 cudaError_t stream_dequantize(const QArgs& a, cudaStream_t st);
 int64_t stream_stats_blocks(const QSpec& q, int sms);           // -1: not supported
-cudaError_t stream_error_stats(const QArgs& a, void* partials, cudaStream_t st);
+// done != nullptr: the kernel's last block also writes the final result to
+// out_dev (done must be zero at launch and counts the finished blocks).
+cudaError_t stream_error_stats(const QArgs& a, void* partials, unsigned int* done, kvq_err* out_dev, cudaStream_t st);
 
 // ---- keep-set selection (select.cu) and compaction (compact.cu)
 struct SelectArgs {

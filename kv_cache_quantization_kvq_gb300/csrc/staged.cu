@@ -19,6 +19,7 @@
 // source load and output store is coalesced; group constants are loaded once
 // per lane item.
 #include <algorithm>
+#include <mutex>
 #include <type_traits>
 
 #include <cudaTypedefs.h>
@@ -45,6 +46,31 @@ __device__ __forceinline__ float ld_meta(const void* p, int64_t i) {
     else if constexpr (DT == KVQ_I8) return (float)static_cast<const int8_t*>(p)[i];
     else return static_cast<const float*>(p)[i];
 }
+// eight consecutive metadata elements (i a multiple of 8, buffer 16-byte aligned)
+template <int DT>
+__device__ __forceinline__ void ld_meta8(const void* p, int64_t i, float (&v)[8]) {
+    if constexpr (DT == KVQ_BF16) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p) + i));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { v[2 * k] = lo_f(ws[k]); v[2 * k + 1] = hi_f(ws[k]); }
+    } else if constexpr (DT == KVQ_I8) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const int8_t*>(p) + i));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[k] = (float)(int8_t)(w.x >> (8 * k));
+            v[k + 4] = (float)(int8_t)(w.y >> (8 * k));
+        }
+    } else if constexpr (DT == KVQ_F32) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i + 4));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+    }
+}
+
 template <int DT>
 __device__ __forceinline__ void st_meta(void* p, int64_t i, float v) {
     if constexpr (DT == KVQ_BF16) static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
@@ -750,9 +776,38 @@ __device__ __forceinline__ void dq_pair_consts(float s, float z, int off, u64& c
     sp = pk(s, s);
 }
 
+// The final fixed-order reduction of the block partials by one block (the
+// last to finish): thread t sums partials t, t + kThr, ... in order, then a
+// fixed tree; the result does not depend on which block ran last.
+__device__ __forceinline__ void finalize_in_block(const Partial* partials, int64_t n, double N, kvq_err* out)
+{
+    __shared__ double f1[kThr], f2[kThr], fm[kThr];
+    double s1 = 0.0, s2 = 0.0, mx = 0.0;
+    for (int64_t i = threadIdx.x; i < n; i += kThr) {
+        s1 += __ldcg(&partials[i].s1);
+        s2 += __ldcg(&partials[i].s2);
+        mx = fmax(mx, __ldcg(&partials[i].mx));
+    }
+    f1[threadIdx.x] = s1; f2[threadIdx.x] = s2; fm[threadIdx.x] = mx;
+    __syncthreads();
+    for (int o = kThr / 2; o > 0; o >>= 1) {
+        if (threadIdx.x < o) {
+            f1[threadIdx.x] += f1[threadIdx.x + o];
+            f2[threadIdx.x] += f2[threadIdx.x + o];
+            fm[threadIdx.x] = fmax(fm[threadIdx.x], fm[threadIdx.x + o]);
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        out->rmse = sqrt(f2[0] / N);
+        out->max_abs = fm[0];
+        out->mean_abs = f1[0] / N;
+    }
+}
+
 template <int BITS, bool ASYM, bool ALONG_T, int RPT, bool STATS, int SDT, int ZDT>
 __global__ void __launch_bounds__(kThr)
-ds_kernel(const QArgs a, int lcpr, int lg, Partial* partials)
+ds_kernel(const QArgs a, int lcpr, int lg, Partial* partials, unsigned int* done, kvq_err* out_dev)
 {
     const QSpec& q = a.q;
     const int off = q.is_signed ? (1 << (BITS - 1)) : 0;
@@ -794,17 +849,18 @@ ds_kernel(const QArgs a, int lcpr, int lg, Partial* partials)
                 u64 cp[4], sp[4];
                 bool fast_t = true;
                 if (ALONG_T) {
-                    // eight per-channel groups shared by the RPT rows
+                    // eight per-channel groups shared by the RPT rows: two 16-byte loads at most
                     const int64_t mi = ((int64_t)o * q.ngroups + (t0 >> lg)) * C + (int64_t)cofs;
+                    float sf[8], zf[8];
+                    ld_meta8<SDT>(a.scale, mi, sf);
+                    if (ASYM) ld_meta8<ZDT>(a.zero, mi, zf);
+                    const float base = 8388608.0f + (float)off;
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
-                        const float s0 = ld_meta<SDT>(a.scale, mi + 2 * p);
-                        const float s1 = ld_meta<SDT>(a.scale, mi + 2 * p + 1);
-                        const float z0 = ASYM ? ld_meta<ZDT>(a.zero, mi + 2 * p) : 0.0f;
-                        const float z1 = ASYM ? ld_meta<ZDT>(a.zero, mi + 2 * p + 1) : 0.0f;
-                        cp[p] = pk(__fadd_rn(8388608.0f + (float)off, z0), __fadd_rn(8388608.0f + (float)off, z1));
-                        sp[p] = pk(s0, s1);
-                        fast_t = fast_t && fabsf(z0) < 0x1p21f && fabsf(z1) < 0x1p21f;
+                        const float z0 = ASYM ? zf[2 * p] : 0.0f, z1 = ASYM ? zf[2 * p + 1] : 0.0f;
+                        cp[p] = add2(pk(z0, z1), pk(base, base));
+                        sp[p] = pk(sf[2 * p], sf[2 * p + 1]);
+                        if (ASYM) fast_t = fast_t && fmaxf(fabsf(z0), fabsf(z1)) < 0x1p21f;
                     }
                 }
                 u64 a1 = 0, a2 = 0;
@@ -873,7 +929,22 @@ ds_kernel(const QArgs a, int lcpr, int lg, Partial* partials)
             }
         }
     }
-    if (STATS) block_reduce_partial(A, partials);
+    if (STATS) {
+        block_reduce_partial(A, partials);
+        if (done) {
+            // the last block to finish reduces every partial in a fixed order
+            __shared__ bool s_last;
+            __threadfence();
+            __syncthreads();
+            const unsigned int nb = gridDim.x * gridDim.y;
+            if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == nb - 1;
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                finalize_in_block(partials, nb, (double)q.outer * (double)q.T * (double)q.C, out_dev);
+            }
+        }
+    }
 }
 
 int log2_exact(int64_t v) {
@@ -1037,40 +1108,97 @@ template <int B, bool A, int S, int Z> struct SqT { static void run(const QArgs&
 template <int B, bool A, int S, int Z> struct SqC { static void run(const QArgs& a, cudaStream_t st) { sq_c_launch<B, A, S, Z>(a, st); } };
 
 // ---- dequantize / statistics geometry
-constexpr int kRpt = 4;
+// rows per lane item: 8 for dequantize along T (group constants shared by
+// more rows), else 4 (fewer registers, more resident warps)
+int ds_rpt(const QSpec& q, bool stats) { return (!stats && q.axis == KVQ_GROUP_ALONG_T && q.g % 8 == 0) ? 8 : 4; }
 
 bool ds_ok(const QSpec& q) {
     if (q.x_dt != KVQ_BF16 || !q.aligned || q.C % 8 != 0 || log2_exact(q.C / 8) < 0 || meta_kind(q) < 0) return false;
     if (log2_exact(q.g) < 0) return false;
-    if (q.axis == KVQ_GROUP_ALONG_T) return q.g % kRpt == 0;
+    if (q.axis == KVQ_GROUP_ALONG_T) return q.g % 4 == 0;
     return q.g % 8 == 0 && q.C % q.g == 0;
 }
 
-dim3 ds_grid(const QSpec& q, int sms) {
+// blocks_per_sm resident blocks on each of sms SMs, at most one item per thread
+dim3 ds_grid(const QSpec& q, int sms, bool stats, int blocks_per_sm = 8) {
     const int lcpr = log2_exact(q.C / 8);
-    const uint64_t items = (uint64_t)((q.T + kRpt - 1) / kRpt) << lcpr;
+    const int rpt = ds_rpt(q, stats);
+    const uint64_t items = (uint64_t)((q.T + rpt - 1) / rpt) << lcpr;
     const unsigned gy = (unsigned)std::max<int64_t>(1, std::min<int64_t>(q.outer, 65535));
-    const uint64_t want_total = (uint64_t)sms * 8;
-    const uint64_t gx = std::max<uint64_t>(1, std::min<uint64_t>((items + kThr - 1) / kThr,
-                                                                  (want_total + gy - 1) / gy));
+    const uint64_t want_total = (uint64_t)sms * (uint64_t)std::max(blocks_per_sm, 1);
+    const uint64_t gx = std::max<uint64_t>(1, std::min<uint64_t>((items + kThr - 1) / kThr, want_total / gy));
     return dim3((unsigned)gx, gy);
 }
+
+// resident blocks per SM of a kernel at kThr threads, queried once per kernel
+// (a small table keyed by the kernel's address)
+template <typename K>
+int resident_blocks(K kernel) {
+    constexpr int kSlots = 256;
+    static const void* keys[kSlots];
+    static int vals[kSlots];
+    static std::mutex mu;
+    const void* key = reinterpret_cast<const void*>(kernel);
+    std::lock_guard<std::mutex> lock(mu);
+    int i = 0;
+    for (; i < kSlots && keys[i]; ++i)
+        if (keys[i] == key) return vals[i];
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThr, 0) != cudaSuccess || b < 1) b = 1;
+    if (i < kSlots) { keys[i] = key; vals[i] = b; }
+    return b;
+}
+
+// Launch context of the statistics pass: block partials, and (when the
+// final reduction is fused) the completion counter and the result.
+struct DsStats { Partial* partials; unsigned int* done; kvq_err* out; };
 
 template <bool STATS>
 struct DsL {
     template <int B, bool A, int S, int Z> struct L {
-        static void run(const QArgs& a, cudaStream_t st) {
+        template <typename K>
+        static void go(K kernel, const QArgs& a, const DsStats& ctx, cudaStream_t st) {
             const QSpec& q = a.q;
-            const dim3 grid = ds_grid(q, sm_count());
-            const int lcpr = log2_exact(q.C / 8), lg = log2_exact(q.g);
-            Partial* partials = static_cast<Partial*>(a.ws);
-            if (q.axis == KVQ_GROUP_ALONG_T)
-                ds_kernel<B, A, true, kRpt, STATS, S, Z><<<grid, kThr, 0, st>>>(a, lcpr, lg, partials);
-            else
-                ds_kernel<B, A, false, kRpt, STATS, S, Z><<<grid, kThr, 0, st>>>(a, lcpr, lg, partials);
+            const dim3 grid = ds_grid(q, sm_count(), STATS, resident_blocks(kernel));
+            kernel<<<grid, kThr, 0, st>>>(a, log2_exact(q.C / 8), log2_exact(q.g), ctx.partials, ctx.done, ctx.out);
+        }
+        static void run(const QArgs& a, const DsStats& ctx, cudaStream_t st) {
+            const QSpec& q = a.q;
+            if (q.axis == KVQ_GROUP_ALONG_T) {
+                if (ds_rpt(q, STATS) == 8) go(ds_kernel<B, A, true, 8, STATS, S, Z>, a, ctx, st);
+                else go(ds_kernel<B, A, true, 4, STATS, S, Z>, a, ctx, st);
+            } else {
+                go(ds_kernel<B, A, false, 4, STATS, S, Z>, a, ctx, st);
+            }
         }
     };
 };
+
+// (bits, meta kind) dispatch for launchers that take the statistics context
+template <template <int, bool, int, int> class L>
+void by_meta_ctx(const QArgs& a, const DsStats& ctx, cudaStream_t st) {
+    const int mk = meta_kind(a.q);
+    switch (a.q.bits) {
+    case 8:
+        if (mk == 0) L<8, true, KVQ_BF16, KVQ_BF16>::run(a, ctx, st);
+        else if (mk == 1) L<8, true, KVQ_F32, KVQ_I8>::run(a, ctx, st);
+        else if (mk == 2) L<8, false, KVQ_BF16, KVQ_NONE>::run(a, ctx, st);
+        else L<8, false, KVQ_F32, KVQ_NONE>::run(a, ctx, st);
+        break;
+    case 4:
+        if (mk == 0) L<4, true, KVQ_BF16, KVQ_BF16>::run(a, ctx, st);
+        else if (mk == 1) L<4, true, KVQ_F32, KVQ_I8>::run(a, ctx, st);
+        else if (mk == 2) L<4, false, KVQ_BF16, KVQ_NONE>::run(a, ctx, st);
+        else L<4, false, KVQ_F32, KVQ_NONE>::run(a, ctx, st);
+        break;
+    default:
+        if (mk == 0) L<2, true, KVQ_BF16, KVQ_BF16>::run(a, ctx, st);
+        else if (mk == 1) L<2, true, KVQ_F32, KVQ_I8>::run(a, ctx, st);
+        else if (mk == 2) L<2, false, KVQ_BF16, KVQ_NONE>::run(a, ctx, st);
+        else L<2, false, KVQ_F32, KVQ_NONE>::run(a, ctx, st);
+        break;
+    }
+}
 
 }  // namespace
 
@@ -1093,22 +1221,20 @@ bool stream_dequant_supported(const QSpec& q, int out_dt) { return out_dt == KVQ
 
 cudaError_t stream_dequantize(const QArgs& a, cudaStream_t st)
 {
-    by_meta<DsL<false>::L>(a, st);
+    by_meta_ctx<DsL<false>::L>(a, DsStats{nullptr, nullptr, nullptr}, st);
     return cudaGetLastError();
 }
 
 int64_t stream_stats_blocks(const QSpec& q, int sms)
 {
     if (!ds_ok(q)) return -1;
-    const dim3 g = ds_grid(q, sms);
+    const dim3 g = ds_grid(q, sms, true);      // an upper bound: at most 8 blocks per SM
     return (int64_t)g.x * g.y;
 }
 
-cudaError_t stream_error_stats(const QArgs& a, void* partials, cudaStream_t st)
+cudaError_t stream_error_stats(const QArgs& a, void* partials, unsigned int* done, kvq_err* out_dev, cudaStream_t st)
 {
-    QArgs b = a;
-    b.ws = partials;
-    by_meta<DsL<true>::L>(b, st);
+    by_meta_ctx<DsL<true>::L>(a, DsStats{static_cast<Partial*>(partials), done, out_dev}, st);
     return cudaGetLastError();
 }
 
