@@ -10,8 +10,9 @@ all inputs resident in HBM when the timed region starts:
   eviction workload (32 heads, history fp32 [64 steps, T 131072], B 2048,
     W 128): H2O select + compaction of K and V, SnapKV select (mean of the
     last 32 steps) + compaction of K and V.
-The L2 is flushed (a 2x-L2 buffer is written) before every phase, outside the
-CUDA-event intervals that time the phases.
+The L2 is flushed (a 2x-L2 buffer is written) before every step, outside the
+CUDA-event interval that times the step; the step's phases run back to back
+(each also bracketed by events, for the per-phase breakdown).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Prints one JSON line (rank 0).
@@ -236,9 +237,8 @@ class Step:
 
     def h2o_compact(self):
         b, H, T, D = self.b, EVICT["heads"], EVICT["T"], EVICT["D"]
-        b.kv_compact(self.EK, b.BF16, H, T, D, self.keep, EVICT["budget"], self.cK, self.stream)
-        b.kv_compact(self.EV, b.BF16, H, T, D, self.keep, EVICT["budget"], self.cV, self.stream)
-        return 2
+        b.kv_compact_kv(self.EK, self.EV, b.BF16, H, T, D, self.keep, EVICT["budget"], self.cK, self.cV, self.stream)
+        return 1
 
     def snapkv_select(self):
         b, H, S, T = self.b, EVICT["heads"], EVICT["steps"], EVICT["T"]
@@ -248,9 +248,9 @@ class Step:
 
     def snapkv_compact(self):
         b, H, T, D = self.b, EVICT["heads"], EVICT["T"], EVICT["D"]
-        b.kv_compact(self.EK, b.BF16, H, T, D, self.skeep, EVICT["budget"], self.scK, self.stream)
-        b.kv_compact(self.EV, b.BF16, H, T, D, self.skeep, EVICT["budget"], self.scV, self.stream)
-        return 2
+        b.kv_compact_kv(self.EK, self.EV, b.BF16, H, T, D, self.skeep, EVICT["budget"], self.scK, self.scV,
+                        self.stream)
+        return 1
 
     PHASES = ("quantize", "dequantize", "error_stats", "h2o_select", "h2o_compact", "snapkv_select",
               "snapkv_compact")
@@ -284,30 +284,64 @@ def run_ours(args, rank, world, local_rank):
     # warm-up
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
+            flush.zero_()
             for ph in phases:
-                flush.zero_()
                 getattr(st, ph)()
     barrier()
 
+    # Per-phase breakdown (not the headline): every phase bracketed by events,
+    # the L2 flushed (a 2x-L2 buffer written) before every step.
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    Kb = max(3, min(args.steps, 200))
+    ev = {ph: [mk() for _ in range(Kb)] for ph in phases}
+    with torch.cuda.stream(stream):
+        for i in range(Kb):
+            flush.zero_()
+            for ph in phases:
+                a, z = ev[ph][i]
+                a.record(stream)
+                getattr(st, ph)()
+                z.record(stream)
+    torch.cuda.synchronize()
+    ph_ms = {ph: statistics.fmean(a.elapsed_time(z) for a, z in ev[ph]) for ph in phases}
+
+    # The step as one sequence: captured once as a CUDA graph (the same C-ABI
+    # calls, recorded on the stream) unless --no-graph; launches counted once.
+    per_step = 0
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for ph in phases:
+                per_step += getattr(st, ph)()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+        torch.cuda.synchronize()
+
+    # Timed region: K steps; before each, the L2 is flushed outside the step's
+    # event interval; the step's phases run back to back.
     K = args.steps
-    ev = {ph: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-          for ph in phases}
+    ev_step = [mk() for _ in range(K)]
     launches = 0
     with ClockSampler(local_rank) as clk:
         barrier()
         t0 = time.perf_counter()
         with torch.cuda.stream(stream):
             for i in range(K):
-                for ph in phases:
-                    flush.zero_()
-                    a, z = ev[ph][i]
-                    a.record(stream)
-                    launches += getattr(st, ph)()
-                    z.record(stream)
+                flush.zero_()
+                ev_step[i][0].record(stream)
+                if graph is not None:
+                    graph.replay()
+                    launches += per_step
+                else:
+                    for ph in phases:
+                        launches += getattr(st, ph)()
+                ev_step[i][1].record(stream)
         barrier()
         wall = time.perf_counter() - t0
-    ph_ms = {ph: statistics.fmean(a.elapsed_time(z) for a, z in ev[ph]) for ph in phases}
-    step_ms = sum(ph_ms.values())
+    step_ms = statistics.fmean(a.elapsed_time(z) for a, z in ev_step)
     if world > 1:
         t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -332,8 +366,11 @@ def run_ours(args, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16/f32 in, int4 codes; f32 arithmetic",
             "data": "synthetic (seeded generators; shapes and distributions of the pages' workloads)",
-            "config": {"workload": WORKLOAD_NAME, "l2": "flushed (2x L2 written) before every phase, outside the timed intervals",
-                       "inputs_resident_in_hbm": True, "parallelism": f"weak: {world} independent replica(s)"},
+            "config": {"workload": WORKLOAD_NAME,
+                       "l2": "flushed (2x L2 written) before every step, outside the timed interval; "
+                             "the step's phases run back to back",
+                       "inputs_resident_in_hbm": True, "parallelism": f"weak: {world} independent replica(s)",
+                       "launch": "CUDA graph of the step's C-ABI calls" if graph is not None else "C-ABI calls"},
             "hbm_frac_of_8TBs": round(value / world / SPEC_HBM_GBS, 4),
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "h2o_tokens_per_s": round(world * tokens / (h2o_ms * 1e-3), 1) if h2o_ms == h2o_ms else None,
@@ -490,6 +527,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="issue the timed steps as plain C-ABI calls instead of replaying a captured CUDA graph")
     ap.add_argument("--only", choices=("all", "kivi", "evict"), default="all",
                     help="time only the KIVI phases or only the eviction phases (profiling)")
     ap.add_argument("--evict-tokens", type=int, default=None,

@@ -191,6 +191,15 @@ KVQ_API kvq_status kv_snapkv_select(const float* hist, int64_t heads, int64_t st
 KVQ_API kvq_status kv_compact(const void* kv, kvq_dtype dtype, int64_t heads, int64_t T, int64_t D,
                       const int32_t* keep, int64_t K, void* out, void* stream);
 
+/* The same compaction for a key and a value cache that share one keep set
+ * (the eviction keeps or drops a token's K and V together), in one launch:
+ * out_k = kv_compact(k), out_v = kv_compact(v).  k and v have the same dtype
+ * and shape [heads][T][D]; out_k and out_v are [heads][K][D].  Errors as for
+ * kv_compact, checked on both tensors before anything is launched. */
+KVQ_API kvq_status kv_compact_kv(const void* k, const void* v, kvq_dtype dtype, int64_t heads, int64_t T,
+                                 int64_t D, const int32_t* keep, int64_t K, void* out_k, void* out_v,
+                                 void* stream);
+
 /* Size of the library's fixed scratch array used by kvq_error_stats_noalloc. */
 #define KVQ_NOALLOC_SCRATCH_BYTES (1 << 20)
 

@@ -64,6 +64,7 @@ def _load() -> ctypes.CDLL:
         "kv_h2o_select": [vp, i64, i64, i64, i64, i64, vp, vp, vp, sz, vp],
         "kv_snapkv_select": [vp, i64, i64, i64, i64, i64, i64, vp, vp, vp, sz, vp],
         "kv_compact": [vp, i32, i64, i64, i64, vp, i64, vp, vp],
+        "kv_compact_kv": [vp, vp, i32, i64, i64, i64, vp, i64, vp, vp, vp],
         "kvq_error_stats_noalloc": [vp, i32, vp, vp, vp, vp, S, P, vp, vp],
     }
     for name, args in sig.items():
@@ -82,7 +83,7 @@ LIB = _load()
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_quantized_sizes", "kvq_quantize", "kvq_dequantize", "kvq_error_stats",
            "kvq_compression_ratio", "kvq_token_compression_ratio", "kv_select_workspace",
-           "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kvq_last_error", "kvq_version",
+           "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kv_compact_kv", "kvq_last_error", "kvq_version",
            "kvq_error_stats_noalloc")
 
 # size of the library's fixed scratch array behind kvq_error_stats_noalloc
@@ -216,6 +217,11 @@ def kv_compact(kv, dtype, heads, T, D, keep, K, out, stream=None):
     _check(LIB.kv_compact(_ptr(kv), dtype, heads, T, D, _ptr(keep), K, _ptr(out), _stream(stream)))
 
 
+def kv_compact_kv(k, v, dtype, heads, T, D, keep, K, out_k, out_v, stream=None):
+    _check(LIB.kv_compact_kv(_ptr(k), _ptr(v), dtype, heads, T, D, _ptr(keep), K, _ptr(out_k), _ptr(out_v),
+                             _stream(stream)))
+
+
 def kvq_last_error() -> str:
     return LIB.kvq_last_error().decode(errors="replace")
 
@@ -311,6 +317,20 @@ def snapkv_select(hist, obs_window: int, budget: int, window: int, workspace=Non
     kv_snapkv_select(hist, H, S, T, obs_window, budget, window, keep, scores, workspace, workspace.numel(),
                      stream)
     return keep, scores
+
+
+def compact_kv(k, v, keep, out_k=None, out_v=None, stream=None):
+    """k, v: CUDA [heads, T, D] of one dtype; keep: int32 [heads, K] -> (k', v') [heads, K, D]."""
+    import torch
+    H, T, D = k.shape
+    K = keep.shape[1]
+    code = {torch.float32: F32, torch.bfloat16: BF16, torch.int8: I8, torch.uint8: I8}[k.dtype]
+    if out_k is None:
+        out_k = torch.empty((H, K, D), dtype=k.dtype, device=k.device)
+    if out_v is None:
+        out_v = torch.empty((H, K, D), dtype=v.dtype, device=v.device)
+    kv_compact_kv(k, v, code, H, T, D, keep, K, out_k, out_v, stream)
+    return out_k, out_v
 
 
 def compact(kv, keep, out=None, stream=None):

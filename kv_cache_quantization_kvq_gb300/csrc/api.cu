@@ -373,4 +373,21 @@ kvq_status kv_compact(const void* kv, kvq_dtype dtype, int64_t heads, int64_t T,
     return cuda_status(kvq::launch_compact(kv, es, heads, T, D, keep, K, out, (cudaStream_t)stream), "kv_compact launch");
 }
 
+kvq_status kv_compact_kv(const void* k, const void* v, kvq_dtype dtype, int64_t heads, int64_t T, int64_t D,
+                         const int32_t* keep, int64_t K, void* out_k, void* out_v, void* stream)
+{
+    const size_t es = dtype_bytes(dtype);
+    if (es == 0) return fail(KVQ_EINVAL, "dtype must be F32, BF16 or I8");
+    if (heads < 0 || T < 0 || D < 0 || T > INT32_MAX || !mul_ok(heads, T, D)) return fail(KVQ_EINVAL, "bad extents");
+    if (K < 0 || K > T) return fail(KVQ_EINVAL, "require 0 <= K <= T");
+    kvq_status s;
+    if ((s = need_ptr(k, (size_t)(heads * T * D), "k")) || (s = need_ptr(v, (size_t)(heads * T * D), "v")) ||
+        (s = need_ptr(keep, (size_t)(heads * K), "keep")) || (s = need_ptr(out_k, (size_t)(heads * K * D), "out_k")) ||
+        (s = need_ptr(out_v, (size_t)(heads * K * D), "out_v")))
+        return s;
+    if ((s = need_align(keep, 4, "keep"))) return s;
+    return cuda_status(kvq::launch_compact_pair(k, v, es, heads, T, D, keep, K, out_k, out_v, (cudaStream_t)stream),
+                       "kv_compact_kv launch");
+}
+
 }  // extern "C"

@@ -87,6 +87,9 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 
 cudaError_t launch_compact(const void* kv, size_t elem, int64_t heads, int64_t T, int64_t D,
                            const int32_t* keep, int64_t K, void* out, cudaStream_t st);
+// K and V with the same keep set in one launch (v, ov may be nullptr)
+cudaError_t launch_compact_pair(const void* k, const void* v, size_t elem, int64_t heads, int64_t T, int64_t D,
+                                const int32_t* keep, int64_t K, void* ok, void* ov, cudaStream_t st);
 
 // number of SMs of the current device (cached per device)
 int sm_count();

@@ -45,13 +45,13 @@ SelectLayout layout(int64_t heads, int64_t T)
     const int64_t nchunks = (T + kCols - 1) / kCols;
     size_t off = 0;
     L.scores = off; off = align256(off + (size_t)(heads * T) * 4);
-    L.hist1 = off;  off = align256(off + (size_t)heads * kBins1 * 4);
+    L.hist1 = off;  off = off + (size_t)heads * kBins1 * 4;
+    L.done = off;   off = align256(off + (size_t)heads * 4);           // zeroed together with hist1
     L.hist2 = off;  off = align256(off + (size_t)heads * kBins2 * 4);
     L.hist3 = off;  off = align256(off + (size_t)heads * kBins3 * 4);
     L.state = off;  off = align256(off + (size_t)heads * 4 * 4);
     L.counts = off; off = align256(off + (size_t)(heads * nchunks) * 2 * 4);
     L.ccount = off; off = align256(off + (size_t)heads * 4);
-    L.done = off;   off = align256(off + (size_t)heads * 4);
     L.cand = off;   off = align256(off + (size_t)(heads * T) * 8);     // room for every key
     L.total = off;
     return L;
@@ -479,28 +479,41 @@ emit_kernel(const float* scores, int64_t T, int64_t rs, int64_t K, int64_t k, in
 constexpr int kFinThreads = 1024;
 constexpr int64_t kBitmapMaxT = int64_t(1) << 19;     // two shared-memory bitmaps of T bits (128 KB)
 
+// CTA (bx, h) takes chunks bx, bx + gridDim.x, ... (kGatherJ at most) of
+// head h: all its loads are issued first, then one block scan and one atomic
+// reserve the CTA's slots in the head's candidate list.
+constexpr int kGatherJ = 4;
+
 __global__ void __launch_bounds__(kThreads)
 gather_kernel(const float* scores, int64_t T, int64_t rs, const uint32_t* state, uint32_t* ccount, uint2* cand,
               int64_t cap, bool vec)
 {
     __shared__ uint32_t s_base;
-    const int64_t h = blockIdx.y;
-    const uint32_t b1 = state[h * 4 + 0];
-    const int64_t col0 = (int64_t)blockIdx.x * kCols + threadIdx.x * 4;
-    float v[4];
-    if (vec && col0 + 3 < rs) {
-        const float4 f = *reinterpret_cast<const float4*>(scores + h * T + col0);
-        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = col0 + j < rs ? scores[h * T + col0 + j] : 0.0f;
-    }
-    uint32_t key[4];
+    const uint32_t h = blockIdx.y;
+    const uint32_t thr = state[h * 4 + 0] << 20;          // lowest key of bin b1
+    const float* sh = scores + (uint64_t)h * (uint64_t)T;
+    const uint32_t rs32 = (uint32_t)rs;                   // T < 2^31
+    uint32_t key[kGatherJ][4];
+    uint32_t is_cand = 0;                                 // bit 4*jj + q
     int n = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        key[j] = score_key(v[j]);
-        n += (col0 + j < rs) && (key[j] >> 20) >= b1;
+    for (int jj = 0; jj < kGatherJ; ++jj) {
+        const uint32_t col0 = (blockIdx.x + jj * gridDim.x) * (uint32_t)kCols + threadIdx.x * 4;
+        float v[4];
+        if (vec && col0 + 3 < rs32) {
+            const float4 f = *reinterpret_cast<const float4*>(sh + col0);
+            v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = col0 + q < rs32 ? sh[col0 + q] : 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            key[jj][q] = score_key(v[q]);
+            const bool c = col0 + q < rs32 && key[jj][q] >= thr;
+            is_cand |= (uint32_t)c << (4 * jj + q);
+            n += c;
+        }
     }
     int total;
     const int excl = block_excl_scan(n, total);
@@ -508,21 +521,26 @@ gather_kernel(const float* scores, int64_t T, int64_t rs, const uint32_t* state,
     if (threadIdx.x == 0) s_base = atomicAdd(&ccount[h], (uint32_t)total);
     __syncthreads();
     uint32_t pos = s_base + (uint32_t)excl;
+    uint2* out = cand + (uint64_t)h * (uint64_t)cap;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int64_t col = col0 + j;
-        if (col < rs && (key[j] >> 20) >= b1) {
-            if (pos < cap) cand[h * cap + pos] = make_uint2(key[j], (uint32_t)col);
-            ++pos;
-        }
+    for (int jj = 0; jj < kGatherJ; ++jj) {
+        const uint32_t col0 = (blockIdx.x + jj * gridDim.x) * (uint32_t)kCols + threadIdx.x * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (is_cand & (1u << (4 * jj + q))) {
+                if (pos < (uint64_t)cap) out[pos] = make_uint2(key[jj][q], col0 + q);
+                ++pos;
+            }
     }
 }
 
 __global__ void __launch_bounds__(kFinThreads)
 finish_kernel(int64_t T, int64_t rs, int64_t k, int64_t K, const uint32_t* state, const uint32_t* ccount,
-              const uint2* cand, int64_t cap, int32_t* keep)
+              const uint2* cand, int64_t cap, int32_t* keep, int64_t cache_cap)
 {
-    extern __shared__ uint32_t bitmap[];                 // ceil(T/32) words, later tie bits reuse hist
+    // dynamic: kept bitmap and tie bitmap (ceil(T/32) words each), then a
+    // copy of the head's candidates when there are at most cache_cap of them
+    extern __shared__ uint32_t bitmap[];
     __shared__ uint32_t hist[kBins2];
     __shared__ int wsum[32];
     __shared__ uint32_t s_val[2];
@@ -530,8 +548,14 @@ finish_kernel(int64_t T, int64_t rs, int64_t k, int64_t K, const uint32_t* state
     const uint32_t b1 = state[h * 4 + 0];
     const int64_t above = (int64_t)state[h * 4 + 1];
     const int64_t m = min((int64_t)ccount[h], cap);
-    const uint2* ch = cand + h * cap;
     const int nwords = (int)((T + 31) / 32);
+    const uint2* ch = cand + h * cap;
+    if (m <= cache_cap) {                 // three passes below read the candidates: keep them on chip
+        uint2* cs = reinterpret_cast<uint2*>(bitmap + 2 * nwords);
+        for (int64_t i = threadIdx.x; i < m; i += kFinThreads) cs[i] = ch[i];
+        __syncthreads();
+        ch = cs;
+    }
     int32_t* kh = keep + h * K;
 
     // levels 2 and 3 among the candidates of bin b1
@@ -712,9 +736,8 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st)
         uint32_t* done = reinterpret_cast<uint32_t*>(ws + L.done);
         uint2* cand = reinterpret_cast<uint2*>(ws + L.cand);
         const bool want_bin = mode == 2;
-        if (want_bin) {
-            cudaError_t e = cudaMemsetAsync(ws + L.hist1, 0, (size_t)H * kBins1 * 4, st);
-            if (e == cudaSuccess) e = cudaMemsetAsync(done, 0, (size_t)H * 4, st);
+        if (want_bin) {       // hist1 and the per-head completion counters are adjacent
+            cudaError_t e = cudaMemsetAsync(ws + L.hist1, 0, L.done + (size_t)H * 4 - L.hist1, st);
             if (e != cudaSuccess) return e;
         }
         const int64_t per_head = std::max<int64_t>(1, std::min<int64_t>(nchunks, ((int64_t)sm_count() * 4 + H - 1) / H));
@@ -722,14 +745,20 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st)
         if (vec) colsum_bin1_kernel<true><<<cgrid, kThreads, 0, st>>>(a, rs, k, scores, hist1, done, state, ccount, want_bin);
         else colsum_bin1_kernel<false><<<cgrid, kThreads, 0, st>>>(a, rs, k, scores, hist1, done, state, ccount, want_bin);
         if (mode == 2) {
-            gather_kernel<<<grid, kThreads, 0, st>>>(scores, T, rs, state, ccount, cand, T, vec);
-            const size_t smem = (size_t)2 * ((T + 31) / 32) * 4;
+            const int64_t rchunks = (rs + kCols - 1) / kCols;
+            const dim3 ggrid((unsigned)std::max<int64_t>(1, (rchunks + kGatherJ - 1) / kGatherJ), (unsigned)H);
+            gather_kernel<<<ggrid, kThreads, 0, st>>>(scores, T, rs, state, ccount, cand, T, vec);
+            const size_t bits_B = (size_t)2 * ((T + 31) / 32) * 4;
+            constexpr size_t kFinDynMax = 200 * 1024;     // + 16.2 KB static stays under 227 KB
+            const int64_t cache_cap = std::min<int64_t>(T, (int64_t)((kFinDynMax - bits_B) / 8));
+            const size_t smem = bits_B + (size_t)cache_cap * 8;
             static size_t attr = 0;
             if (smem > attr) {                       // static + dynamic may exceed the 48 KB default
                 cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
                 attr = smem;
             }
-            finish_kernel<<<(unsigned)H, kFinThreads, smem, st>>>(T, rs, k, K, state, ccount, cand, T, a.keep);
+            finish_kernel<<<(unsigned)H, kFinThreads, smem, st>>>(T, rs, k, K, state, ccount, cand, T, a.keep,
+                                                                  cache_cap);
         } else {
             emit_kernel<<<grid, kThreads, 0, st>>>(scores, T, rs, K, k, mode, state, counts, a.keep);
         }

@@ -33,7 +33,7 @@ def declared_symbols():
 
 def test_library_exports_every_declared_symbol(kb):
     declared = declared_symbols()
-    assert len(declared) == 13
+    assert len(declared) == 14
     for name in declared:
         assert hasattr(kb.LIB, name), name
     assert declared == set(kb.EXPORTS)
@@ -163,6 +163,17 @@ def test_calls_rejected_before_launch(kb):
     with pytest.raises(kb.KvqError):
         kb.kv_compact(fake, kb.BF16, 4, 100, 128, None, 10, fake, 0)
     assert "NULL" in kb.kvq_last_error()
+    # the K+V form checks both tensors and both outputs
+    for K in (-1, 101):
+        with pytest.raises(kb.KvqError):
+            kb.kv_compact_kv(fake, fake, kb.BF16, 4, 100, 128, fake, K, fake, fake, 0)
+    for args in ((None, fake, fake, fake), (fake, None, fake, fake), (fake, fake, None, fake), (fake, fake, fake, None)):
+        k, v, ok, ov = args
+        with pytest.raises(kb.KvqError):
+            kb.kv_compact_kv(k, v, kb.BF16, 4, 100, 128, fake, 10, ok, ov, 0)
+        assert "NULL" in kb.kvq_last_error()
+    with pytest.raises(kb.KvqError):
+        kb.kv_compact_kv(fake, fake, kb.F32, 4, 100, 128, fake + 2, 10, fake, fake, 0)
 
 
 def test_misaligned_buffers_rejected(kb):

@@ -130,6 +130,33 @@ def test_compact(b, dtype, D):
     assert np.array_equal(to_host(out), want)
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("bf16", 32), ("f32", 16), ("f32", 256), ("bf16", 512),
+                                     ("i8", 40), ("bf16", 3)])
+def test_compact_kv_pair(b, dtype, D):
+    """K and V through one call: rows of 64 B .. 1 KB take the batched row
+    kernel, other sizes the per-piece kernel; ragged K, a permuted keep row,
+    and keep entries outside [0, T) (zero rows)."""
+    import torch
+    rng = np.random.default_rng(D * 3 + len(dtype))
+    H, T, K = 3, 500, 77
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "i8": torch.int8}[dtype]
+    k = torch.from_numpy(rng.standard_normal((H, T, D)).astype(np.float32) * 10).to(tdt).cuda()
+    v = torch.from_numpy(rng.standard_normal((H, T, D)).astype(np.float32) * 10).to(tdt).cuda()
+    keep = np.sort(rng.choice(T, (H, K)), axis=1).astype(np.int32)
+    keep[1] = rng.permutation(T)[:K]
+    keep[2, 5] = -1
+    keep[2, 40] = T
+    ok, ov = b.compact_kv(k, v, torch.from_numpy(keep).cuda())
+    torch.cuda.synchronize()
+    for src, got in ((k, ok), (v, ov)):
+        host = to_host(src)
+        want = O.compact(host, np.clip(keep, 0, T - 1))
+        g = to_host(got)
+        bad = (keep < 0) | (keep >= T)
+        want[bad] = 0
+        assert np.array_equal(g, want)
+
+
 def test_compact_out_of_range_rows_are_zero(b):
     import torch
     kv = torch.arange(2 * 10 * 16, dtype=torch.float32, device="cuda").view(2, 10, 16)
