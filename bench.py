@@ -309,19 +309,61 @@ def run_ours(args, rank, world, local_rank):
     # calls, recorded on the stream) unless --no-graph; launches counted once.
     per_step = 0
     graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for ph in phases:
-                per_step += getattr(st, ph)()
+    kivi_ph = [ph for ph in phases if ph in kivi_bytes()]
+    evict_ph = [ph for ph in phases if ph not in kivi_bytes()]
+    overlap = (not args.serial_rows) and bool(kivi_ph) and bool(evict_ph)
+
+    def capture(two_branches):
+        nonlocal per_step
+        per_step = 0
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        with torch.cuda.graph(g, stream=stream):
+            if two_branches:
+                # the KIVI rows and the eviction rows share no buffer: two
+                # branches of the graph, joined at the end of the step
+                fork = torch.cuda.Event()
+                fork.record(stream)
+                side.wait_event(fork)
+                for ph in kivi_ph:
+                    per_step += getattr(st, ph)()
+                st.stream = side
+                for ph in evict_ph:
+                    per_step += getattr(st, ph)()
+                st.stream = stream
+                join = torch.cuda.Event()
+                join.record(side)
+                stream.wait_event(join)
+            else:
+                for ph in phases:
+                    per_step += getattr(st, ph)()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             for _ in range(3):
-                graph.replay()
+                g.replay()
         torch.cuda.synchronize()
+        return g
+
+    def time_graph(g, n):
+        evs = [mk() for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                flush.zero_()
+                evs[i][0].record(stream)
+                g.replay()
+                evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.fmean(a.elapsed_time(z) for a, z in evs)
+
+    serial_ms = None
+    if not args.no_graph:
+        if overlap:          # the rows in sequence, for reference (not the headline)
+            serial_ms = time_graph(capture(False), max(3, min(args.steps, 200)))
+        graph = capture(overlap)
 
     # Timed region: K steps; before each, the L2 is flushed outside the step's
-    # event interval; the step's phases run back to back.
+    # event interval; the step replays the graph (the KIVI and the eviction
+    # rows as two concurrent branches unless --serial-rows).
     K = args.steps
     ev_step = [mk() for _ in range(K)]
     launches = 0
@@ -367,10 +409,10 @@ def run_ours(args, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16/f32 in, int4 codes; f32 arithmetic",
             "data": "synthetic (seeded generators; shapes and distributions of the pages' workloads)",
             "config": {"workload": WORKLOAD_NAME,
-                       "l2": "flushed (2x L2 written) before every step, outside the timed interval; "
-                             "the step's phases run back to back",
+                       "l2": "flushed (2x L2 written) before every step, outside the timed interval",
                        "inputs_resident_in_hbm": True, "parallelism": f"weak: {world} independent replica(s)",
-                       "launch": "CUDA graph of the step's C-ABI calls" if graph is not None else "C-ABI calls"},
+                       "launch": ("CUDA graph of the step's C-ABI calls" if graph is not None else "C-ABI calls") +
+                                 ("; KIVI and eviction rows as two concurrent branches" if graph is not None and overlap else "")},
             "hbm_frac_of_8TBs": round(value / world / SPEC_HBM_GBS, 4),
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "h2o_tokens_per_s": round(world * tokens / (h2o_ms * 1e-3), 1) if h2o_ms == h2o_ms else None,
@@ -381,6 +423,7 @@ def run_ours(args, rank, world, local_rank):
                          "unit": "GB/s", "frac": round(sel_gbs / peak, 4) if sel_gbs else None,
                          "peak_kind": f"of {peak_kind}",
                          "bytes_per_launch": sel_B, "traffic": ncu_traffic()},
+            "ms_per_step_rows_in_sequence": round(serial_ms, 5) if serial_ms else None,
             "gpu_launches": launches,
             "wall_s_timed_region": round(wall, 3),
             "clocks": clk.summary(),
@@ -527,6 +570,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--serial-rows", action="store_true",
+                    help="run the KIVI rows and the eviction rows one after the other instead of as two "
+                         "concurrent branches of the step graph")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue the timed steps as plain C-ABI calls instead of replaying a captured CUDA graph")
     ap.add_argument("--only", choices=("all", "kivi", "evict"), default="all",

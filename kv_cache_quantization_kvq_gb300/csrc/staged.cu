@@ -71,6 +71,31 @@ __device__ __forceinline__ void ld_meta8(const void* p, int64_t i, float (&v)[8]
     }
 }
 
+// the same from shared memory (plain loads)
+template <int DT>
+__device__ __forceinline__ void ld_meta8_smem(const unsigned char* p, int i, float (&v)[8]) {
+    if constexpr (DT == KVQ_BF16) {
+        const uint4 w = *reinterpret_cast<const uint4*>(p + 2 * i);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { v[2 * k] = lo_f(ws[k]); v[2 * k + 1] = hi_f(ws[k]); }
+    } else if constexpr (DT == KVQ_I8) {
+        const uint2 w = *reinterpret_cast<const uint2*>(p + i);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[k] = (float)(int8_t)(w.x >> (8 * k));
+            v[k + 4] = (float)(int8_t)(w.y >> (8 * k));
+        }
+    } else if constexpr (DT == KVQ_F32) {
+        const float4 a = *reinterpret_cast<const float4*>(p + 4 * i);
+        const float4 b = *reinterpret_cast<const float4*>(p + 4 * i + 16);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+    }
+}
+
 template <int DT>
 __device__ __forceinline__ void st_meta(void* p, int64_t i, float v) {
     if constexpr (DT == KVQ_BF16) static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
@@ -947,6 +972,215 @@ ds_kernel(const QArgs a, int lcpr, int lg, Partial* partials, unsigned int* done
     }
 }
 
+// ======================================================================
+// dequantize / statistics along T, warp-specialised (bf16, C = 128, g in
+// {16, 32, 64}).  A chunk is one quantized group tile of an outer slice: the
+// producer warp bulk-copies its codes [g rows x 16*BITS B], the 128 scales
+// and zero points and, for the statistics, the source tile [g x 128] bf16
+// into one ring stage.  Stage s belongs to warp pair s % P (two stages per
+// pair); the two warps of a pair take one 64-channel half each: lane = 8
+// channels x every fourth row, with the group constants of its channels read
+// from the stage once per tile.  Dequantize writes x_hat rows straight from
+// registers (16 B per lane, 128 B per 8 lanes) and copies the residual rows;
+// statistics accumulate as in ds_kernel, and the last CTA reduces the block
+// partials in a fixed order.
+// ======================================================================
+template <int BITS, int G, bool STATS, int SDT, int ZDT>
+struct DtShape {
+    static constexpr int CR = G;                                     // rows per chunk: one group tile
+    static constexpr uint32_t kXB = STATS ? (uint32_t)G * 256u : 0u;  // the source tile (statistics)
+    static constexpr int WT = STATS ? 4 : 2;                          // consumer warps sharing one stage
+    static constexpr uint32_t kCodeRowB = 16u * BITS;
+    static constexpr uint32_t kCodesB = (uint32_t)CR * kCodeRowB;
+    static constexpr uint32_t kSB = 128u * (SDT == KVQ_F32 ? 4u : 2u);
+    static constexpr uint32_t kZB = ZDT == KVQ_NONE ? 0u : 128u * (ZDT == KVQ_I8 ? 1u : ZDT == KVQ_F32 ? 4u : 2u);
+    static constexpr uint32_t offCodes = kXB, offS = kXB + kCodesB, offZ = offS + kSB;
+    static constexpr uint32_t kStage = (offZ + kZB + 127u) / 128u * 128u;
+    static constexpr int kConsumers = 16;                            // consumer warps (+ 1 producer)
+    static constexpr int kTeams = kConsumers / WT;                   // a team of WT warps owns two stages
+    static constexpr int kStages = 2 * kTeams;
+    static constexpr int kThreads = (kConsumers + 1) * 32;
+    static constexpr int kSmem = kStages * (int)kStage + 2 * kStages * 8;
+    static_assert(kSmem <= 227 * 1024, "ring does not fit in shared memory");
+};
+
+template <int BITS, bool ASYM, int G, bool STATS, int SDT, int ZDT>
+__global__ void __launch_bounds__(DtShape<BITS, G, STATS, SDT, ZDT>::kThreads, 1)
+wds_t_kernel(const QArgs a, Partial* partials, unsigned int* done, kvq_err* out_dev)
+{
+    using L = DtShape<BITS, G, STATS, SDT, ZDT>;
+    using W = typename CodeWord<BITS>::T;
+    constexpr int C = 128;
+    constexpr int P = L::kTeams, S = L::kStages, WT = L::WT, NCW = L::kConsumers;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * L::kStage);
+    uint64_t* empty = full + S;
+
+    constexpr int CR = L::CR, CPG = G / CR;                // rows per chunk, chunks per group
+    const QSpec& q = a.q;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ng = (uint32_t)q.ngroups;
+    const uint32_t nchunks = (uint32_t)q.outer * ng * CPG; // < 2^31, checked by the dispatcher
+    const uint32_t Tq32 = (uint32_t)q.Tq, T32 = (uint32_t)q.T;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], WT);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const uint32_t first = blockIdx.x, step = gridDim.x;
+    // chunk c -> (outer o, group k, first row, rows); the tail chunks of a
+    // short last group may hold no rows (only the group constants are copied)
+    auto geom = [&](uint32_t c, uint32_t& o, uint32_t& grp, uint32_t& row0, uint32_t& nrows) {
+        grp = c / CPG;
+        o = grp / ng;
+        const uint32_t k = grp - o * ng;
+        row0 = k * (uint32_t)G + (c - grp * CPG) * (uint32_t)CR;
+        nrows = row0 < Tq32 ? min((uint32_t)CR, Tq32 - row0) : 0u;
+    };
+
+    if (warp == NCW) {
+        // ---- producer
+        if (lane != 0) return;
+        const unsigned char* codes = static_cast<const unsigned char*>(a.codes);
+        uint32_t n = 0;
+        for (;; ++n) {
+            const uint32_t c = first + n * step;
+            if (c >= nchunks) break;
+            const int s = (int)(n % S);
+            if (n >= (uint32_t)S && !mbar_wait(&empty[s], ((n / S) - 1) & 1u)) break;
+            uint32_t o, grp, row0, nrows;
+            geom(c, o, grp, row0, nrows);
+            unsigned char* st = smem + s * L::kStage;
+            mbar_expect_tx(&full[s], nrows * (L::kXB ? 256u : 0u) + nrows * L::kCodeRowB + L::kSB + L::kZB);
+            if (STATS && nrows)
+                bulk_g2s(st, static_cast<const __nv_bfloat16*>(a.x) + ((uint64_t)o * T32 + row0) * C, nrows * 256u, &full[s]);
+            if (nrows)
+                bulk_g2s(st + L::offCodes, codes + ((uint64_t)o * Tq32 + row0) * L::kCodeRowB, nrows * L::kCodeRowB, &full[s]);
+            bulk_g2s(st + L::offS, static_cast<const unsigned char*>(a.scale) + (uint64_t)grp * L::kSB, L::kSB, &full[s]);
+            if (L::kZB)
+                bulk_g2s(st + L::offZ, static_cast<const unsigned char*>(a.zero) + (uint64_t)grp * L::kZB, L::kZB, &full[s]);
+        }
+        for (uint32_t i = n > (uint32_t)S ? n - S : 0; i < n; ++i) mbar_wait(&full[i % S], (i / S) & 1u);
+        return;
+    }
+
+    // ---- consumers: team p of WT warps; warp wt of the team, lane = 8 channels
+    // (c8) x rows r0 + 2*WT*i with r0 = 2*wt + (lane >> 4)
+    const int pair = warp / WT, wt = warp - pair * WT;
+    const int c8 = lane & 15, rq = 2 * wt + (lane >> 4);
+    constexpr int RSTEP = 2 * WT;
+    const int chan0 = c8 * 8;
+    const int off = q.is_signed ? (1 << (BITS - 1)) : 0;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    Acc2 A;
+    for (uint32_t j = pair;; j += P) {
+        const uint32_t c = first + j * step;
+        if (c >= nchunks) break;
+        const int s = (int)(j % S);
+        // on a timeout (recorded in g_kvq_wait_timeouts) leave the loop but still reach the barriers below
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (j / S) & 1u))) break;
+        const unsigned char* st = smem + s * L::kStage;
+        uint32_t o, grp, row0, nr;
+        geom(c, o, grp, row0, nr);
+        const int nrows = (int)nr;
+        // the group constants of this lane's eight channels
+        float sf[8], zf[8];
+        ld_meta8_smem<SDT>(st + L::offS, chan0, sf);
+        if (ASYM) ld_meta8_smem<ZDT>(st + L::offZ, chan0, zf);
+        u64 cp[4], sp[4];
+        bool fast = true;
+        const float base = 8388608.0f + (float)off;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float z0 = ASYM ? zf[2 * p] : 0.0f, z1 = ASYM ? zf[2 * p + 1] : 0.0f;
+            cp[p] = add2(pk(z0, z1), pk(base, base));
+            sp[p] = pk(sf[2 * p], sf[2 * p + 1]);
+            if (ASYM) fast = fast && fmaxf(fabsf(z0), fabsf(z1)) < 0x1p21f;
+        }
+        const unsigned char* cbase = st + L::offCodes + (uint32_t)(chan0 / 8) * BITS;
+        const unsigned char* xbase = st + chan0 * 2;
+        __nv_bfloat16* obase = out + ((uint64_t)o * T32 + row0) * C + chan0;
+        u64 a1 = 0, a2 = 0;
+        auto row = [&](int r) {
+            W cw = *reinterpret_cast<const W*>(cbase + (uint32_t)r * L::kCodeRowB);
+            uint32_t u[8];
+            unpack_biased8<BITS>(q.is_signed ? flip_signs<BITS>(cw) : cw, u);
+            const uint4 xw = STATS ? *reinterpret_cast<const uint4*>(xbase + (uint32_t)r * 256u) : make_uint4(0, 0, 0, 0);
+            uint4 ow;
+            if (fast) ow = dq8<STATS>(u, cp, sp, xw, a1, a2, A.mxb);
+            else ow = dq8_slow<STATS>(u, off, zf, sf, xw, a1, a2, A.mxb);
+            if (!STATS) *reinterpret_cast<uint4*>(obase + (uint64_t)r * C) = ow;
+        };
+        if (nrows == CR) {
+#pragma unroll 4
+            for (int i = 0; i < CR / RSTEP; ++i) row(rq + RSTEP * i);
+        } else {
+            for (int i = 0; i < CR / RSTEP; ++i)
+                if (rq + RSTEP * i < nrows) row(rq + RSTEP * i);
+        }
+        if (STATS) A.fold(a1, a2);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    constexpr int kCons = NCW * 32;                        // consumer threads
+    if (!STATS) {
+        // residual rows: resid [outer][R][C] -> out rows Tq .. T-1, 16 bytes per item
+        const uint64_t nres = (uint64_t)q.outer * (uint64_t)q.R * (C / 8);
+        const uint4* rs = static_cast<const uint4*>(a.resid);
+        for (uint64_t i = (uint64_t)blockIdx.x * kCons + threadIdx.x; i < nres; i += (uint64_t)gridDim.x * kCons) {
+            const uint64_t rr = i / (C / 8), piece = i % (C / 8);
+            const uint64_t o = rr / (uint64_t)q.R, t = rr % (uint64_t)q.R;
+            *reinterpret_cast<uint4*>(out + ((o * T32 + Tq32 + t) * C + piece * 8)) = rs[i];
+        }
+        return;
+    }
+
+    // ---- block partial over the consumer warps, then the fused final reduction
+    __shared__ double w1[NCW], w2[NCW], wm[NCW];
+    __shared__ bool s_last;
+    double d1 = (double)A.s1 - (double)A.e1, d2 = (double)A.s2 - (double)A.e2, dm = (double)__uint_as_float(A.mxb);
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+        d1 += __shfl_xor_sync(0xFFFFFFFFu, d1, o2);
+        d2 += __shfl_xor_sync(0xFFFFFFFFu, d2, o2);
+        dm = fmax(dm, __shfl_xor_sync(0xFFFFFFFFu, dm, o2));
+    }
+    if (lane == 0) { w1[warp] = d1; w2[warp] = d2; wm[warp] = dm; }
+    asm volatile("bar.sync 1, %0;" ::"r"(kCons) : "memory");
+    if (threadIdx.x == 0) {
+        Partial pp = {0.0, 0.0, 0.0};
+        for (int i = 0; i < NCW; ++i) { pp.s1 += w1[i]; pp.s2 += w2[i]; pp.mx = fmax(pp.mx, wm[i]); }
+        partials[blockIdx.x] = pp;
+        __threadfence();
+        s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kCons) : "memory");
+    if (!s_last || warp != 0) return;
+    __threadfence();
+    // warp 0 of the last CTA: partials in a fixed order (lane l takes l, l+32, ...), then a fixed tree
+    double f1 = 0.0, f2 = 0.0, fm = 0.0;
+    for (uint32_t i = lane; i < gridDim.x; i += 32) {
+        f1 += __ldcg(&partials[i].s1);
+        f2 += __ldcg(&partials[i].s2);
+        fm = fmax(fm, __ldcg(&partials[i].mx));
+    }
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+        f1 += __shfl_xor_sync(0xFFFFFFFFu, f1, o2);
+        f2 += __shfl_xor_sync(0xFFFFFFFFu, f2, o2);
+        fm = fmax(fm, __shfl_xor_sync(0xFFFFFFFFu, fm, o2));
+    }
+    if (lane == 0) {
+        const double N = (double)q.outer * (double)q.T * (double)q.C;
+        out_dev->rmse = sqrt(f2 / N);
+        out_dev->max_abs = fm;
+        out_dev->mean_abs = f1 / N;
+    }
+}
+
 int log2_exact(int64_t v) {
     int l = 0;
     while ((int64_t(1) << l) < v) ++l;
@@ -1202,6 +1436,39 @@ void by_meta_ctx(const QArgs& a, const DsStats& ctx, cudaStream_t st) {
 
 }  // namespace
 
+// ---- warp-specialised dequantize / statistics along T
+bool wds_t_ok(const QSpec& q) {
+    return q.axis == KVQ_GROUP_ALONG_T && q.x_dt == KVQ_BF16 && q.aligned && q.C == 128 &&
+           (q.g == 16 || q.g == 32 || q.g == 64) && meta_kind(q) >= 0 && q.Tq > 0 &&
+           q.outer * q.ngroups * 2 < (int64_t(1) << 31) && q.outer * q.T < (int64_t(1) << 31);
+}
+
+template <bool STATS>
+struct WdsL {
+    template <int B, bool A, int S, int Z> struct L {
+        template <int G>
+        static void go(const QArgs& a, const DsStats& ctx, cudaStream_t st) {
+            using Sh = DtShape<B, G, STATS, S, Z>;
+            auto kernel = wds_t_kernel<B, A, G, STATS, S, Z>;
+            static bool attr = false;
+            if (!attr) {
+                cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+                attr = true;
+            }
+            const uint64_t nchunks = (uint64_t)a.q.outer * a.q.ngroups * (G / Sh::CR);
+            const unsigned grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(nchunks, (uint64_t)sm_count()));
+            kernel<<<grid, Sh::kThreads, Sh::kSmem, st>>>(a, ctx.partials, ctx.done, ctx.out);
+        }
+        static void run(const QArgs& a, const DsStats& ctx, cudaStream_t st) {
+            switch (a.q.g) {
+            case 16: go<16>(a, ctx, st); break;
+            case 32: go<32>(a, ctx, st); break;
+            default: go<64>(a, ctx, st); break;
+            }
+        }
+    };
+};
+
 // ---- entry points (see kvq_internal.h)
 
 bool staged_quantize_supported(const QSpec& q)
@@ -1221,7 +1488,8 @@ bool stream_dequant_supported(const QSpec& q, int out_dt) { return out_dt == KVQ
 
 cudaError_t stream_dequantize(const QArgs& a, cudaStream_t st)
 {
-    by_meta_ctx<DsL<false>::L>(a, DsStats{nullptr, nullptr, nullptr}, st);
+    if (wds_t_ok(a.q)) by_meta_ctx<WdsL<false>::L>(a, DsStats{nullptr, nullptr, nullptr}, st);
+    else by_meta_ctx<DsL<false>::L>(a, DsStats{nullptr, nullptr, nullptr}, st);
     return cudaGetLastError();
 }
 
@@ -1234,7 +1502,9 @@ int64_t stream_stats_blocks(const QSpec& q, int sms)
 
 cudaError_t stream_error_stats(const QArgs& a, void* partials, unsigned int* done, kvq_err* out_dev, cudaStream_t st)
 {
-    by_meta_ctx<DsL<true>::L>(a, DsStats{static_cast<Partial*>(partials), done, out_dev}, st);
+    // the warp-specialised kernel always fuses the final reduction (needs done)
+    if (done && wds_t_ok(a.q)) by_meta_ctx<WdsL<true>::L>(a, DsStats{static_cast<Partial*>(partials), done, out_dev}, st);
+    else by_meta_ctx<DsL<true>::L>(a, DsStats{static_cast<Partial*>(partials), done, out_dev}, st);
     return cudaGetLastError();
 }
 
