@@ -199,6 +199,7 @@ class Step:
         self.skeep = torch.empty_like(self.keep)
         self.selB = b.kv_select_workspace(H, T)
         self.sel_ws = torch.empty(self.selB, dtype=torch.uint8, device=dev)
+        self.sel_ws2 = torch.empty(self.selB, dtype=torch.uint8, device=dev)    # SnapKV's own
         self.cK = torch.empty((H, EVICT["budget"], D), dtype=torch.bfloat16, device=dev)
         self.cV = torch.empty_like(self.cK)
         self.scK = torch.empty_like(self.cK)
@@ -243,7 +244,7 @@ class Step:
     def snapkv_select(self):
         b, H, S, T = self.b, EVICT["heads"], EVICT["steps"], EVICT["T"]
         b.kv_snapkv_select(self.hist, H, S, T, EVICT["obs"], EVICT["budget"], EVICT["window"], self.skeep, None,
-                           self.sel_ws, self.selB, self.stream)
+                           self.sel_ws2, self.selB, self.stream)
         return 3
 
     def snapkv_compact(self):
@@ -309,31 +310,33 @@ def run_ours(args, rank, world, local_rank):
     # calls, recorded on the stream) unless --no-graph; launches counted once.
     per_step = 0
     graph = None
-    kivi_ph = [ph for ph in phases if ph in kivi_bytes()]
-    evict_ph = [ph for ph in phases if ph not in kivi_bytes()]
-    overlap = (not args.serial_rows) and bool(kivi_ph) and bool(evict_ph)
+    # independent chains of rows (they share no buffer): KIVI, H2O, SnapKV
+    chains = [c for c in ([ph for ph in phases if ph in kivi_bytes()],
+                          [ph for ph in phases if ph.startswith("h2o")],
+                          [ph for ph in phases if ph.startswith("snapkv")]) if c]
+    overlap = (not args.serial_rows) and len(chains) > 1
 
-    def capture(two_branches):
+    def capture(branches):
         nonlocal per_step
         per_step = 0
         g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(device=dev)
+        sides = [torch.cuda.Stream(device=dev) for _ in chains[1:]]
         with torch.cuda.graph(g, stream=stream):
-            if two_branches:
-                # the KIVI rows and the eviction rows share no buffer: two
-                # branches of the graph, joined at the end of the step
+            if branches:
+                # one branch of the graph per chain, joined at the end of the step
                 fork = torch.cuda.Event()
                 fork.record(stream)
-                side.wait_event(fork)
-                for ph in kivi_ph:
-                    per_step += getattr(st, ph)()
-                st.stream = side
-                for ph in evict_ph:
-                    per_step += getattr(st, ph)()
+                for sd in sides:
+                    sd.wait_event(fork)
+                for chain, sd in zip(chains, [stream] + sides):
+                    st.stream = sd
+                    for ph in chain:
+                        per_step += getattr(st, ph)()
                 st.stream = stream
-                join = torch.cuda.Event()
-                join.record(side)
-                stream.wait_event(join)
+                for sd in sides:
+                    join = torch.cuda.Event()
+                    join.record(sd)
+                    stream.wait_event(join)
             else:
                 for ph in phases:
                     per_step += getattr(st, ph)()
@@ -362,8 +365,8 @@ def run_ours(args, rank, world, local_rank):
         graph = capture(overlap)
 
     # Timed region: K steps; before each, the L2 is flushed outside the step's
-    # event interval; the step replays the graph (the KIVI and the eviction
-    # rows as two concurrent branches unless --serial-rows).
+    # event interval; the step replays the graph (the KIVI, H2O and SnapKV
+    # rows as concurrent branches unless --serial-rows).
     K = args.steps
     ev_step = [mk() for _ in range(K)]
     launches = 0
@@ -412,7 +415,7 @@ def run_ours(args, rank, world, local_rank):
                        "l2": "flushed (2x L2 written) before every step, outside the timed interval",
                        "inputs_resident_in_hbm": True, "parallelism": f"weak: {world} independent replica(s)",
                        "launch": ("CUDA graph of the step's C-ABI calls" if graph is not None else "C-ABI calls") +
-                                 ("; KIVI and eviction rows as two concurrent branches" if graph is not None and overlap else "")},
+                                 ("; the KIVI, H2O and SnapKV rows as concurrent branches" if graph is not None and overlap else "")},
             "hbm_frac_of_8TBs": round(value / world / SPEC_HBM_GBS, 4),
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "h2o_tokens_per_s": round(world * tokens / (h2o_ms * 1e-3), 1) if h2o_ms == h2o_ms else None,
@@ -571,8 +574,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--serial-rows", action="store_true",
-                    help="run the KIVI rows and the eviction rows one after the other instead of as two "
-                         "concurrent branches of the step graph")
+                    help="run the KIVI, H2O and SnapKV rows one after the other instead of as concurrent "
+                         "branches of the step graph")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue the timed steps as plain C-ABI calls instead of replaying a captured CUDA graph")
     ap.add_argument("--only", choices=("all", "kivi", "evict"), default="all",
