@@ -73,6 +73,27 @@ def evict_bytes():
 
 # ---------------------------------------------------------------- helpers
 
+def rank_seed_offset(rank: int) -> int:
+    """Seed offset of a rank's synthetic inputs: rank 0 keeps the workload's
+    own seeds, every other rank draws a batch of its own."""
+    return 1000 * rank
+
+
+def reduce_max_over_ranks(x: float, world: int, device) -> float:
+    """Max of a per-rank value over all ranks (the timing rule: the slowest
+    rank decides); a no-op for one rank.  Uses the default process group."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: float, step_ms: float, world: int) -> float:
+    """Whole-job throughput: every rank moved bytes_per_rank_step in step_ms."""
+    return world * bytes_per_rank_step / (step_ms * 1e-3) / 1e9
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -164,12 +185,13 @@ class ClockSampler:
 class Step:
     """Device buffers and the launches of one step, through the C ABI."""
 
-    def __init__(self, b, dev, stream, only="all"):
+    def __init__(self, b, dev, stream, only="all", rank=0):
         import torch
         from kv_cache_quantization_kvq_gb300 import workloads as W
         self.b, self.dev, self.stream = b, dev, stream
         outer = KIVI["batch"] * KIVI["heads"]
         self.kshape = (outer, KIVI["T"], KIVI["D"])
+        self.seed_off = rank_seed_offset(rank)     # every rank its own synthetic batch (weak scaling)
         if only in ("all", "kivi"):
             self._init_kivi(b, dev, W)
         if only in ("all", "evict"):
@@ -178,7 +200,7 @@ class Step:
 
     def _init_kivi(self, b, dev, W):
         import torch
-        self.K, self.V = W.kivi_kv(dev, seed=2, batch=KIVI["batch"], heads=KIVI["heads"], T=KIVI["T"], D=KIVI["D"])
+        self.K, self.V = W.kivi_kv(dev, seed=2 + self.seed_off, batch=KIVI["batch"], heads=KIVI["heads"], T=KIVI["T"], D=KIVI["D"])
         self.qpK = b.QParams.asym(4, 0, 15, axis=b.ALONG_T, group=KIVI["g"], residual=KIVI["R"],
                                   scale_dtype=b.BF16, zero_dtype=b.BF16)
         self.qpV = b.QParams.asym(4, 0, 15, axis=b.ALONG_C, group=KIVI["g"], residual=KIVI["R"],
@@ -193,7 +215,7 @@ class Step:
     def _init_evict(self, b, dev, W):
         import torch
         H, S, T, D = EVICT["heads"], EVICT["steps"], EVICT["T"], EVICT["D"]
-        self.hist, self.EK, self.EV = W.eviction_inputs(dev, seed=5, heads=H, steps=S, T=T, D=D,
+        self.hist, self.EK, self.EV = W.eviction_inputs(dev, seed=5 + self.seed_off, heads=H, steps=S, T=T, D=D,
                                                         window=EVICT["window"])
         self.keep = torch.empty((H, EVICT["budget"]), dtype=torch.int32, device=dev)
         self.skeep = torch.empty_like(self.keep)
@@ -267,7 +289,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        st = Step(b, dev, stream, args.only)
+        st = Step(b, dev, stream, args.only, rank)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
@@ -386,13 +408,9 @@ def run_ours(args, rank, world, local_rank):
                 ev_step[i][1].record(stream)
         barrier()
         wall = time.perf_counter() - t0
-    step_ms = statistics.fmean(a.elapsed_time(z) for a, z in ev_step)
-    if world > 1:
-        t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = reduce_max_over_ranks(statistics.fmean(a.elapsed_time(z) for a, z in ev_step), world, dev)
     total_bytes = sum(pbytes.values())
-    value = world * total_bytes / (step_ms * 1e-3) / 1e9
+    value = whole_job_gbs(total_bytes, step_ms, world)
 
     # sanity of the step's outputs (not timed): finite statistics
     torch.cuda.synchronize()
