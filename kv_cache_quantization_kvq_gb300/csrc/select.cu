@@ -46,7 +46,7 @@ SelectLayout layout(int64_t heads, int64_t T)
     size_t off = 0;
     L.scores = off; off = align256(off + (size_t)(heads * T) * 4);
     L.hist1 = off;  off = off + (size_t)heads * kBins1 * 4;
-    L.done = off;   off = align256(off + (size_t)heads * 4);           // zeroed together with hist1
+    L.done = off;   off = align256(off + (size_t)heads * 8);           // two counters per head, zeroed with hist1
     L.hist2 = off;  off = align256(off + (size_t)heads * kBins2 * 4);
     L.hist3 = off;  off = align256(off + (size_t)heads * kBins3 * 4);
     L.state = off;  off = align256(off + (size_t)heads * 4 * 4);
@@ -249,9 +249,10 @@ colsum_bin1_kernel(const SelectArgs a, int64_t rs, int64_t k, float* scores, uin
 // ---------------------------------------------------------------- block scans
 
 // exclusive prefix sum over the 256 threads of a block, in thread order
-__device__ __forceinline__ int block_excl_scan(int v, int& total)
+template <int NT>
+__device__ __forceinline__ int block_excl_scan_n(int v, int& total)
 {
-    __shared__ int ws[kThreads / 32];
+    __shared__ int ws[NT / 32];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int x = v;
 #pragma unroll
@@ -262,20 +263,22 @@ __device__ __forceinline__ int block_excl_scan(int v, int& total)
     if (lane == 31) ws[w] = x;
     __syncthreads();
     if (w == 0) {
-        int y = lane < kThreads / 32 ? ws[lane] : 0;
+        int y = lane < NT / 32 ? ws[lane] : 0;
 #pragma unroll
-        for (int o = 1; o < kThreads / 32; o <<= 1) {
+        for (int o = 1; o < NT / 32; o <<= 1) {
             const int z = __shfl_up_sync(0xFFFFFFFFu, y, o);
             if (lane >= o) y += z;
         }
-        if (lane < kThreads / 32) ws[lane] = y;
+        if (lane < NT / 32) ws[lane] = y;
     }
     __syncthreads();
     const int incl = x + (w > 0 ? ws[w - 1] : 0);
-    total = ws[kThreads / 32 - 1];
+    total = ws[NT / 32 - 1];
     __syncthreads();
     return incl - v;
 }
+
+__device__ __forceinline__ int block_excl_scan(int v, int& total) { return block_excl_scan_n<kThreads>(v, total); }
 
 // ---------------------------------------------------------------- radix select
 
@@ -534,9 +537,10 @@ gather_kernel(const float* scores, int64_t T, int64_t rs, const uint32_t* state,
     }
 }
 
-__global__ void __launch_bounds__(kFinThreads)
-finish_kernel(int64_t T, int64_t rs, int64_t k, int64_t K, const uint32_t* state, const uint32_t* ccount,
-              const uint2* cand, int64_t cap, int32_t* keep, int64_t cache_cap)
+// The keep set of head h from its candidate list (kFinThreads threads).
+__device__ __forceinline__ void finish_head(int64_t h, int64_t T, int64_t rs, int64_t k, int64_t K,
+                                            const uint32_t* state, int64_t m, const uint2* ch, int32_t* keep,
+                                            int64_t cache_cap)
 {
     // dynamic: kept bitmap and tie bitmap (ceil(T/32) words each), then a
     // copy of the head's candidates when there are at most cache_cap of them
@@ -544,22 +548,53 @@ finish_kernel(int64_t T, int64_t rs, int64_t k, int64_t K, const uint32_t* state
     __shared__ uint32_t hist[kBins2];
     __shared__ int wsum[32];
     __shared__ uint32_t s_val[2];
-    const int64_t h = blockIdx.x;
-    const uint32_t b1 = state[h * 4 + 0];
-    const int64_t above = (int64_t)state[h * 4 + 1];
-    const int64_t m = min((int64_t)ccount[h], cap);
+    const uint32_t b1 = __ldcg(&state[h * 4 + 0]);
+    const int64_t above = (int64_t)__ldcg(&state[h * 4 + 1]);
     const int nwords = (int)((T + 31) / 32);
-    const uint2* ch = cand + h * cap;
     if (m <= cache_cap) {                 // three passes below read the candidates: keep them on chip
         uint2* cs = reinterpret_cast<uint2*>(bitmap + 2 * nwords);
-        for (int64_t i = threadIdx.x; i < m; i += kFinThreads) cs[i] = ch[i];
+        for (int64_t i = threadIdx.x; i < m; i += kFinThreads) cs[i] = __ldcg(&ch[i]);
         __syncthreads();
         ch = cs;
     }
     int32_t* kh = keep + h * K;
 
-    // levels 2 and 3 among the candidates of bin b1
-    uint32_t prefix = b1, rem = (uint32_t)(k - above);
+    // Kept: every candidate above bin b1, plus the best `need` of bin b1 by
+    // (key desc, index asc).  When bin b1 holds at most kFinThreads keys they
+    // are ranked directly (each against all others); otherwise radix levels
+    // 2 and 3 find the exact k-th key and the ties are taken in index order.
+    const uint32_t need = (uint32_t)(k - above);
+    __shared__ uint2 binc[kFinThreads];
+    __shared__ int s_nb;
+    if (threadIdx.x == 0) s_nb = 0;
+    for (int i = threadIdx.x; i < nwords; i += kFinThreads) bitmap[i] = 0;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < m; i += kFinThreads) {
+        const uint2 c = ch[i];
+        const uint32_t bin = c.x >> 20;
+        if (bin > b1) {
+            atomicOr(&bitmap[c.y >> 5], 1u << (c.y & 31));
+        } else if (bin == b1) {
+            const int slot = atomicAdd(&s_nb, 1);
+            if (slot < kFinThreads) binc[slot] = c;
+        }
+    }
+    __syncthreads();
+    const int nb = s_nb;
+    if (nb <= kFinThreads) {
+        if ((int)threadIdx.x < nb) {
+            const uint2 me = binc[threadIdx.x];
+            uint32_t rank = 0;
+            for (int j2 = 0; j2 < nb; ++j2) {
+                const uint2 o = binc[j2];
+                rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
+            }
+            if (rank < need) atomicOr(&bitmap[me.y >> 5], 1u << (me.y & 31));
+        }
+        __syncthreads();
+    } else {
+    // radix levels 2 and 3 among the candidates of bin b1
+    uint32_t prefix = b1, rem = need;
     for (int level = 2; level <= 3; ++level) {
         const int nbins = level == 2 ? kBins2 : kBins3;
         for (int b = threadIdx.x; b < nbins; b += kFinThreads) hist[b] = 0;
@@ -613,21 +648,18 @@ finish_kernel(int64_t T, int64_t rs, int64_t k, int64_t K, const uint32_t* state
         __syncthreads();
     }
     const uint32_t kth = prefix;
-    const uint32_t need = rem;
-
-    // bitmap of kept candidates: keys above T*, then the lowest-index ties
-    for (int i = threadIdx.x; i < nwords; i += kFinThreads) bitmap[i] = 0;
-    __syncthreads();
+    const uint32_t tneed = rem;
+    // keys of bin b1 above T* are kept; ties of T* by index
     uint32_t* ties = bitmap + nwords;                    // second bitmap for the ties
     for (int i = threadIdx.x; i < nwords; i += kFinThreads) ties[i] = 0;
     __syncthreads();
     for (int64_t i = threadIdx.x; i < m; i += kFinThreads) {
         const uint2 c = ch[i];
+        if ((c.x >> 20) != b1) continue;
         if (c.x > kth) atomicOr(&bitmap[c.y >> 5], 1u << (c.y & 31));
         else if (c.x == kth) atomicOr(&ties[c.y >> 5], 1u << (c.y & 31));
     }
     __syncthreads();
-    // keep the first `need` tie bits in index order
     {
         const int wpt = (nwords + kFinThreads - 1) / kFinThreads;
         const int w0 = (int)threadIdx.x * wpt;
@@ -658,11 +690,12 @@ finish_kernel(int64_t T, int64_t rs, int64_t k, int64_t K, const uint32_t* state
             while (tw) {
                 const int bit = __ffs(tw) - 1;
                 tw &= tw - 1;
-                if ((uint32_t)before < need) bitmap[w0 + j] |= 1u << bit;
+                if ((uint32_t)before < tneed) bitmap[w0 + j] |= 1u << bit;
                 ++before;
             }
         }
         __syncthreads();
+    }
     }
     // scan the kept bitmap in index order and write the indices ascending
     {
@@ -704,6 +737,88 @@ finish_kernel(int64_t T, int64_t rs, int64_t k, int64_t K, const uint32_t* state
     for (int64_t i = rs + threadIdx.x; i < T; i += kFinThreads) kh[k + (i - rs)] = (int32_t)i;
 }
 
+__global__ void __launch_bounds__(kFinThreads)
+finish_kernel(int64_t T, int64_t rs, int64_t k, int64_t K, const uint32_t* state, const uint32_t* ccount,
+              const uint2* cand, int64_t cap, int32_t* keep, int64_t cache_cap)
+{
+    const int64_t h = blockIdx.x;
+    finish_head(h, T, rs, k, K, state, min((int64_t)ccount[h], cap), cand + h * cap, keep, cache_cap);
+}
+
+// Gather and finish in one launch: kGFParts CTAs per head (kFinThreads
+// threads each) gather the candidates of a quarter of the head's scores --
+// all loads issued first, keys kept in registers, one block scan and one
+// atomic per CTA -- and the last CTA of the head to finish (done2[h], zeroed
+// before the column sums) builds the head's keep set from the list.
+constexpr int kGFParts = 4;
+constexpr int kGFMaxJ = 8;                // 4-column groups per thread at most: rs <= 4 * 8 * 4 * kFinThreads
+
+__global__ void __launch_bounds__(kFinThreads, 1)
+gather_finish_kernel(const float* scores, int64_t T, int64_t rs, int64_t k, int64_t K, const uint32_t* state,
+                     uint32_t* ccount, uint32_t* done2, uint2* cand, int64_t cap, int32_t* keep, int64_t cache_cap,
+                     int jpt)
+{
+    __shared__ uint32_t s_base;
+    __shared__ bool s_last;
+    const uint32_t h = blockIdx.y;
+    const uint32_t thr = __ldg(&state[h * 4 + 0]) << 20;        // lowest key of bin b1
+    const float* sh = scores + (uint64_t)h * (uint64_t)T;
+    const uint32_t rs32 = (uint32_t)rs;
+    const uint32_t span = (uint32_t)jpt * 4u * kFinThreads;       // columns per part
+    const uint32_t base = blockIdx.x * span + threadIdx.x * 4u;
+    uint32_t key[kGFMaxJ][4];
+    uint32_t is_cand = 0;                                         // bit 4*j + q
+    int n = 0;
+#pragma unroll
+    for (int j = 0; j < kGFMaxJ; ++j) {
+        if (j < jpt) {
+            const uint32_t col0 = base + (uint32_t)j * 4u * kFinThreads;
+            float v[4];
+            if (col0 + 3 < rs32) {
+                const float4 f = __ldcg(reinterpret_cast<const float4*>(sh + col0));
+                v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = col0 + q < rs32 ? __ldcg(sh + col0 + q) : 0.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                key[j][q] = score_key(v[q]);
+                const bool c = col0 + q < rs32 && key[j][q] >= thr;
+                is_cand |= (uint32_t)c << (4 * j + q);
+                n += c;
+            }
+        }
+    }
+    int total;
+    const int excl = block_excl_scan_n<kFinThreads>(n, total);
+    if (threadIdx.x == 0) s_base = total ? atomicAdd(&ccount[h], (uint32_t)total) : 0u;
+    __syncthreads();
+    uint32_t pos = s_base + (uint32_t)excl;
+    uint2* out = cand + (uint64_t)h * (uint64_t)cap;
+#pragma unroll
+    for (int j = 0; j < kGFMaxJ; ++j) {
+        if (is_cand & (0xFu << (4 * j))) {
+            const uint32_t col0 = base + (uint32_t)j * 4u * kFinThreads;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (is_cand & (1u << (4 * j + q))) {
+                    if (pos < (uint64_t)cap) out[pos] = make_uint2(key[j][q], col0 + q);
+                    ++pos;
+                }
+        }
+    }
+    // the last part of the head builds the keep set
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&done2[h], 1u) == kGFParts - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int64_t m = min((int64_t)__ldcg(&ccount[h]), cap);
+    finish_head(h, T, rs, k, K, state, m, out, keep, cache_cap);
+}
+
 }  // namespace
 
 size_t select_workspace(int64_t heads, int64_t T) { return layout(heads, T).total; }
@@ -737,7 +852,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st)
         uint2* cand = reinterpret_cast<uint2*>(ws + L.cand);
         const bool want_bin = mode == 2;
         if (want_bin) {       // hist1 and the per-head completion counters are adjacent
-            cudaError_t e = cudaMemsetAsync(ws + L.hist1, 0, L.done + (size_t)H * 4 - L.hist1, st);
+            cudaError_t e = cudaMemsetAsync(ws + L.hist1, 0, L.done + (size_t)H * 8 - L.hist1, st);
             if (e != cudaSuccess) return e;
         }
         const int64_t per_head = std::max<int64_t>(1, std::min<int64_t>(nchunks, ((int64_t)sm_count() * 4 + H - 1) / H));
@@ -745,20 +860,32 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st)
         if (vec) colsum_bin1_kernel<true><<<cgrid, kThreads, 0, st>>>(a, rs, k, scores, hist1, done, state, ccount, want_bin);
         else colsum_bin1_kernel<false><<<cgrid, kThreads, 0, st>>>(a, rs, k, scores, hist1, done, state, ccount, want_bin);
         if (mode == 2) {
-            const int64_t rchunks = (rs + kCols - 1) / kCols;
-            const dim3 ggrid((unsigned)std::max<int64_t>(1, (rchunks + kGatherJ - 1) / kGatherJ), (unsigned)H);
-            gather_kernel<<<ggrid, kThreads, 0, st>>>(scores, T, rs, state, ccount, cand, T, vec);
             const size_t bits_B = (size_t)2 * ((T + 31) / 32) * 4;
-            constexpr size_t kFinDynMax = 200 * 1024;     // + 16.2 KB static stays under 227 KB
+            constexpr size_t kFinDynMax = 190 * 1024;     // + ~25 KB static stays under 227 KB
             const int64_t cache_cap = std::min<int64_t>(T, (int64_t)((kFinDynMax - bits_B) / 8));
             const size_t smem = bits_B + (size_t)cache_cap * 8;
-            static size_t attr = 0;
-            if (smem > attr) {                       // static + dynamic may exceed the 48 KB default
-                cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                attr = smem;
+            const int64_t per_part = (rs + kGFParts - 1) / kGFParts;
+            const int jpt = (int)std::max<int64_t>(1, (per_part + 4 * kFinThreads - 1) / (4 * kFinThreads));
+            if (jpt <= kGFMaxJ && vec && T >= 4) {
+                static size_t attr_gf = 0;
+                if (smem > attr_gf) {
+                    cudaFuncSetAttribute(gather_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                    attr_gf = smem;
+                }
+                gather_finish_kernel<<<dim3(kGFParts, (unsigned)H), kFinThreads, smem, st>>>(
+                    scores, T, rs, k, K, state, ccount, done + H, cand, T, a.keep, cache_cap, jpt);
+            } else {
+                const int64_t rchunks = (rs + kCols - 1) / kCols;
+                const dim3 ggrid((unsigned)std::max<int64_t>(1, (rchunks + kGatherJ - 1) / kGatherJ), (unsigned)H);
+                gather_kernel<<<ggrid, kThreads, 0, st>>>(scores, T, rs, state, ccount, cand, T, vec);
+                static size_t attr = 0;
+                if (smem > attr) {                       // static + dynamic may exceed the 48 KB default
+                    cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                    attr = smem;
+                }
+                finish_kernel<<<(unsigned)H, kFinThreads, smem, st>>>(T, rs, k, K, state, ccount, cand, T, a.keep,
+                                                                      cache_cap);
             }
-            finish_kernel<<<(unsigned)H, kFinThreads, smem, st>>>(T, rs, k, K, state, ccount, cand, T, a.keep,
-                                                                  cache_cap);
         } else {
             emit_kernel<<<grid, kThreads, 0, st>>>(scores, T, rs, K, k, mode, state, counts, a.keep);
         }
