@@ -439,7 +439,7 @@ def run_ours(args, rank, world, local_rank):
             "h2o_tokens_per_s": round(world * tokens / (h2o_ms * 1e-3), 1) if h2o_ms == h2o_ms else None,
             "phases": {ph: {"ms": round(ph_ms[ph], 5), "GB/s": round(pbytes[ph] / (ph_ms[ph] * 1e-3) / 1e9, 1),
                             "bytes": pbytes[ph]} for ph in phases},
-            "roofline": {"kernel": "kv_h2o_select (colsum_bin1_kernel + gather_kernel + finish_kernel)",
+            "roofline": {"kernel": "kv_h2o_select (colsum_bin1_kernel + gather_finish_kernel)",
                          "bound": "hbm", "achieved": round(sel_gbs, 1) if sel_gbs else None, "peak": peak,
                          "unit": "GB/s", "frac": round(sel_gbs / peak, 4) if sel_gbs else None,
                          "peak_kind": f"of {peak_kind}",
