@@ -457,7 +457,106 @@ def run_ours(args, rank, world, local_rank):
             result["e2e"] = run_e2e(b, st, stream, dev, args, total_bytes, world)
         if not args.no_cpu_baseline and world == 1:
             result["cpu_baseline"] = cpu_baseline(min_seconds=args.cpu_seconds)
+        if args.configs:
+            try:
+                result["configs"] = run_configs(b, dev, stream, flush)
+            except Exception as exc:          # the table is informational; keep the contract line
+                result["configs"] = {"error": f"{type(exc).__name__}: {exc}"}
     return result
+
+
+# ---------------------------------------------------------------- per-config table
+
+def quant_bytes(shape, x_es, cB, sB, zB, rB):
+    """Algorithmic bytes of one quantize (read x, write codes + metadata +
+    residual) -- the same total for dequantize, reversed -- and of one
+    error-statistics pass (read x + codes + metadata; the residual's error is
+    zero by construction)."""
+    outer, T, C = shape
+    x = outer * T * C * x_es
+    return x + cB + sB + zB + rB, x + cB + sB + zB
+
+
+def run_configs(b, dev, stream, flush, runs=20):
+    """Median over `runs` (L2 flushed before each) of every op of the large
+    configurations: KIVI INT4 (2), full-model INT8 per channel (3), the
+    group / bit-width sweep (4), H2O / SnapKV (5); the tiny one (1) in us."""
+    import torch
+    from kv_cache_quantization_kvq_gb300 import workloads as W
+    peak, _ = measured_peak()
+    out = {}
+
+    def med(fn):
+        ts = []
+        with torch.cuda.stream(stream):
+            fn()
+            for _ in range(runs):
+                flush.zero_()
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                z.record(stream)
+                ts.append((a, z))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(z) for a, z in ts)
+
+    def entry(ms, nbytes):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac_of_8TBs": round(gbs / SPEC_HBM_GBS, 3),
+                "frac_of_measured": round(gbs / peak, 3), "bytes": nbytes}
+
+    def qdq(tag, named, qp, stats=True):
+        shape = tuple(named[0][1].shape)
+        for name, x in named:
+            qt, ws = b.alloc_quantized(shape, b.BF16, qp, dev)
+            cB, sB, zB, rB = (t.numel() for t in (qt.codes, qt.scale, qt.zero, qt.resid))
+            qb, sb = quant_bytes(shape, 2, cB, sB, zB, rB)
+            outx = torch.empty_like(x)
+            e = torch.zeros(3, dtype=torch.float64, device=dev)
+            q_ms = med(lambda: b.quantize(x, qp, out=qt, workspace=ws, stream=stream))
+            d_ms = med(lambda: b.dequantize(qt, out=outx, stream=stream))
+            out[f"{tag}/{name}/quantize"] = entry(q_ms, qb)
+            out[f"{tag}/{name}/dequantize"] = entry(d_ms, qb)
+            if stats:
+                s_ms = med(lambda: b.error_stats(x, qt, workspace=ws, stream=stream, out_dev=e))
+                out[f"{tag}/{name}/error_stats"] = entry(s_ms, sb)
+            out[f"{tag}/{name}/bytes_per_number"] = round((cB + sB) / (shape[0] * shape[1] * shape[2]), 6)
+            del qt, ws, outx
+
+    # 2: KIVI INT4
+    K, V = W.kivi_kv(dev, seed=2)
+    for axis, x, name in ((b.ALONG_T, K, "K"), (b.ALONG_C, V, "V")):
+        qp = b.QParams.asym(4, 0, 15, axis=axis, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
+        qdq("2_kivi_int4", [(name, x)], qp)
+    del K, V
+    # 3: full model INT8, per channel over all tokens
+    K, V = W.fullmodel_kv(dev, seed=3)
+    qdq("3_fullmodel_int8", [("K", K), ("V", V)], b.QParams.sym(8, axis=b.ALONG_T, group=0))
+    del K, V
+    # 4: sweep, per token, INT4 / INT2, g in {32, 64, 128}
+    K, V = W.sweep_kv(dev, seed=4)
+    for bits in (4, 2):
+        for g in (32, 64, 128):
+            qdq(f"4_sweep_int{bits}_g{g}", [("K", K), ("V", V)],
+                b.QParams.sym(bits, axis=b.ALONG_C, group=g, scale_dtype=b.BF16), stats=False)
+    del K, V
+    torch.cuda.empty_cache()
+    # 1: tiny (launch-bound: microseconds only)
+    x, hist = W.tiny_inputs(0)
+    xd = torch.from_numpy(x).reshape(1, 256, 128).to(dev)
+    hd = torch.from_numpy(hist).to(dev)
+    for qn, qp in (("int8_sym", b.QParams.sym(8, axis=b.ALONG_T, group=0)),
+                   ("int8_asym", b.QParams.asym(8, -128, 127, axis=b.ALONG_T, group=0, zero_dtype=b.I8)),
+                   ("int4_g32", b.QParams.sym(4, axis=b.ALONG_T, group=32))):
+        qt, ws = b.alloc_quantized((1, 256, 128), b.F32, qp, dev)
+        o = torch.empty_like(xd)
+        e = torch.zeros(3, dtype=torch.float64, device=dev)
+        out[f"1_tiny/{qn}/quantize_us"] = round(1e3 * med(lambda: b.quantize(xd, qp, out=qt, workspace=ws, stream=stream)), 2)
+        out[f"1_tiny/{qn}/dequantize_us"] = round(1e3 * med(lambda: b.dequantize(qt, out=o, stream=stream)), 2)
+        out[f"1_tiny/{qn}/error_stats_us"] = round(1e3 * med(lambda: b.error_stats(xd, qt, workspace=ws, stream=stream, out_dev=e)), 2)
+    out["1_tiny/h2o_select_us"] = round(1e3 * med(lambda: b.h2o_select(hd, 64, 16, stream=stream)), 2)
+    out["1_tiny/snapkv_select_us"] = round(1e3 * med(lambda: b.snapkv_select(hd, 32, 64, 16, stream=stream)), 2)
+    return out
 
 
 def run_e2e(b, st, stream, dev, args, total_bytes, world):
@@ -591,6 +690,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", action="store_true",
+                    help="add the per-configuration table (tiny, KIVI INT4, full-model INT8, g/bit sweep)")
     ap.add_argument("--serial-rows", action="store_true",
                     help="run the KIVI, H2O and SnapKV rows one after the other instead of as concurrent "
                          "branches of the step graph")
