@@ -712,7 +712,9 @@ cudaError_t fast_quantize(const QArgs& a, cudaStream_t st)
         }
         return ok ? cudaGetLastError() : cudaErrorInvalidValue;
     }
-    // long groups along T
+    // long groups along T: one cluster per group and channel block, else a
+    // stats pass and an apply pass through the workspace
+    if (cluster_quantize(a, st)) return cudaGetLastError();
     const uint32_t ncb = (uint32_t)(q.C / 64);
     const uint32_t nsl = (uint32_t)((q.g + kLongRows - 1) / kLongRows);
     const size_t n_keys = (size_t)(q.outer * q.ngroups * q.C);

@@ -59,6 +59,14 @@ cudaError_t fast_dequantize(const QArgs& a, cudaStream_t st);
 int64_t fast_stats_blocks(const QSpec& q, int sms);   // -1: not supported
 cudaError_t fast_error_stats(const QArgs& a, void* partials, cudaStream_t st);
 
+// ---- quantize, groups along T longer than one tile, one thread-block
+// cluster per (slice, group, 64 channels) (cluster.cu)
+bool cluster_quantize_supported(const QSpec& q);
+bool cluster_quantize(const QArgs& a, cudaStream_t st);         // false: not handled
+
+// The driver's cuTensorMapEncodeTiled, looked up once (nullptr: unavailable).
+void* tensor_map_encode_fn();
+
 // ---- staged quantize and streaming dequantize / statistics (staged.cu)
 bool staged_quantize_supported(const QSpec& q);
 bool staged_quantize(const QArgs& a, cudaStream_t st);          // false: not handled

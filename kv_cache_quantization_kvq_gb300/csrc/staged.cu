@@ -1471,6 +1471,8 @@ struct WdsL {
 
 // ---- entry points (see kvq_internal.h)
 
+void* tensor_map_encode_fn() { return reinterpret_cast<void*>(tensor_map_encoder()); }
+
 bool staged_quantize_supported(const QSpec& q)
 {
     return q.axis == KVQ_GROUP_ALONG_T ? staged_t_ok(q) : staged_c_ok(q);

@@ -176,6 +176,42 @@ def test_along_t_fast(b, case):
     check_case(b, xin, xd, oq)
 
 
+# Long groups along T (one scale per channel over hundreds to thousands of
+# tokens): bf16 sources take the cluster kernel, where 1 to 16 CTAs share one
+# group of 64 channels (ceil(group / 512) CTAs, or ceil(group / 1024) where
+# clusters of 16 are unavailable) and persistent clusters walk the units
+# through a ring of shared-memory slots; groups beyond 8192 tokens take the
+# two-pass path.  Ragged last groups (some CTAs of a cluster get no rows),
+# residual windows, several channel blocks, and (last two) many more units
+# than resident clusters, so every ring slot is refilled several times.
+LONG_T_CASES = [
+    # bits, mode (qmin, qmax) or None, g, T, R, C, kind, outer
+    (8, None, 0, 4100, 4, 128, "normal", 2),
+    (8, None, 0, 8192, 0, 192, "normal", 2),
+    (4, (0, 15), 1000, 2600, 7, 128, "normal", 2),
+    (2, None, 3000, 6100, 0, 64, "normal", 2),
+    (4, None, 5000, 5100, 50, 128, "wide", 2),
+    (8, (-128, 127), 700, 1500, 3, 64, "const", 2),
+    (4, (-8, 7), 2048, 4096, 0, 64, "ties", 2),
+    (8, (0, 255), 0, 9000, 0, 64, "normal", 2),
+    (8, (0, 255), 600, 1300, 0, 2048, "normal", 8),
+    (8, None, 0, 8192, 0, 512, "normal", 4),
+]
+
+
+@pytest.mark.parametrize("case", LONG_T_CASES, ids=str)
+def test_along_t_long_groups(b, case):
+    bits, qr, g, T, R, C, kind, outer = case
+    rng = np.random.default_rng(zlib.crc32(repr(case).encode()))
+    xin = make_input(rng, (outer, T, C), O.BF16, kind)
+    if qr is None:
+        oq = sym(bits, axis=O.ALONG_T, group=g, residual=R, scale_dtype=O.F32 if bits == 8 else O.BF16)
+    else:
+        oq = O.QParams.asym(bits, qr[0], qr[1], axis=O.ALONG_T, group=g, residual=R,
+                            scale_dtype=O.F32 if qr[0] < 0 else O.BF16, zero_dtype=O.I8 if qr[0] < 0 else O.BF16)
+    check_case(b, xin, O.BF16, oq)
+
+
 @pytest.mark.parametrize("C", [8, 24, 136])
 def test_along_t_partial_channel_block(b, C):
     rng = np.random.default_rng(C)
