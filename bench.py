@@ -104,10 +104,15 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The sources of the dominant call's kernels (colsum_bin1_kernel and
+# gather_finish_kernel): a change to either invalidates its ncu traffic.
+DOMINANT_SOURCES = ("select.cu", "kvq_device.cuh")
+
+
 def source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kv_cache_quantization_kvq_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in DOMINANT_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

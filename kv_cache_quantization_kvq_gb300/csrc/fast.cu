@@ -485,7 +485,7 @@ dc_kernel(const QArgs a, int lcpr, Partial* partials)
             for (int k = 0; k < 8; ++k) xw[k] = __ldcs(xs + k);
         }
         uint4 ow[8];
-        u64 a1 = 0, a2 = 0;
+        TileAcc ta;
 #pragma unroll
         for (int gg = 0; gg < GPL; ++gg) {
             const int64_t mi = (int64_t)qrow * gpr + (G >= 64 ? (int64_t)ch / LPG : (int64_t)ch * GPL + gg);
@@ -501,17 +501,17 @@ dc_kernel(const QArgs a, int lcpr, Partial* partials)
                 uint32_t u[8];
                 unpack_biased8<BITS>(q.is_signed ? flip_signs<BITS>(cw[wi]) : cw[wi], u);
                 if (fast) {
-                    ow[wi] = dq8<STATS>(u, cp, sp, xw[wi], a1, a2, A.mxb);
+                    ow[wi] = dq8<STATS>(u, cp, sp, xw[wi], ta, A.mxb);
                 } else {
                     float zs[8], ss[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) { zs[j] = zp; ss[j] = s; }
-                    ow[wi] = dq8_slow<STATS>(u, off, zs, ss, xw[wi], a1, a2, A.mxb);
+                    ow[wi] = dq8_slow<STATS>(u, off, zs, ss, xw[wi], ta, A.mxb);
                 }
             }
         }
         if (STATS) {
-            A.fold(a1, a2);
+            A.fold(ta);
         } else {
             uint4* dst = reinterpret_cast<uint4*>(out + ((uint64_t)row * q.C + (uint64_t)ch * 64));
 #pragma unroll
@@ -591,18 +591,18 @@ dt_kernel(const QArgs a, uint32_t ncb, uint32_t nsl, Partial* partials)
                 if (STATS) xw[j] = __ldcs(reinterpret_cast<const uint4*>(x + (((uint64_t)o * q.T + t) * q.C + c0)));
             }
         }
-        u64 a1 = 0, a2 = 0;
+        TileAcc ta;
 #pragma unroll
         for (int j = 0; j < RPT; ++j) {
             const int64_t t = tb + j;
             if (t >= gend) continue;
             uint32_t u[8];
             unpack_biased8<BITS>(q.is_signed ? flip_signs<BITS>(cw[j]) : cw[j], u);
-            const uint4 ow = fast ? dq8<STATS>(u, cp, sp, xw[j], a1, a2, A.mxb)
-                                  : dq8_slow<STATS>(u, off, zsf, sf, xw[j], a1, a2, A.mxb);
+            const uint4 ow = fast ? dq8<STATS>(u, cp, sp, xw[j], ta, A.mxb)
+                                  : dq8_slow<STATS>(u, off, zsf, sf, xw[j], ta, A.mxb);
             if (!STATS) *reinterpret_cast<uint4*>(out + (((uint64_t)o * q.T + t) * q.C + c0)) = ow;
         }
-        if (STATS) A.fold(a1, a2);
+        if (STATS) A.fold(ta);
     }
     if (STATS) block_reduce_partial(A, partials);
 }

@@ -126,7 +126,13 @@ __device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0
 
 constexpr uint32_t kBfPosInf2 = 0x7F807F80u, kBfNegInf2 = 0xFF80FF80u;
 
-// Kahan-compensated float32 pair accumulators, one max as float bits.
+// Per-tile sums of |d| and d^2 on float pairs, one accumulator per pair of
+// a lane's eight channels, so consecutive rows do not chain on one register.
+struct TileAcc {
+    u64 a1[4] = {0, 0, 0, 0}, a2[4] = {0, 0, 0, 0};
+};
+
+// Kahan-compensated float32 accumulators of the tile sums, one max as float bits.
 struct Acc2 {
     float s1 = 0.0f, e1 = 0.0f, s2 = 0.0f, e2 = 0.0f;
     uint32_t mxb = 0;
@@ -136,17 +142,36 @@ struct Acc2 {
         e = __fsub_rn(__fsub_rn(t, s), y);
         s = t;
     }
-    __device__ __forceinline__ void fold(u64 a1, u64 a2) {   // a tile's pair sums
-        kahan(s1, e1, __fadd_rn(lo_of(a1), hi_of(a1)));
-        kahan(s2, e2, __fadd_rn(lo_of(a2), hi_of(a2)));
+    __device__ __forceinline__ void fold(const TileAcc& t) {   // a tile's pair sums
+        const u64 p1 = add2(add2(t.a1[0], t.a1[1]), add2(t.a1[2], t.a1[3]));
+        const u64 p2 = add2(add2(t.a2[0], t.a2[1]), add2(t.a2[2], t.a2[3]));
+        kahan(s1, e1, __fadd_rn(lo_of(p1), hi_of(p1)));
+        kahan(s2, e2, __fadd_rn(lo_of(p2), hi_of(p2)));
     }
 };
+
+// The statistics of eight differences (four float pairs): sums into the
+// tile accumulators, the max of |d| (as float bits, |d| >= 0) into mxb.
+__device__ __forceinline__ void acc8(const u64 (&d)[4], TileAcc& t, uint32_t& mxb) {
+    uint32_t ab[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        ab[2 * j] = lo_bits(d[j]) & 0x7FFFFFFFu;
+        ab[2 * j + 1] = hi_bits(d[j]) & 0x7FFFFFFFu;
+        t.a1[j] = add2(t.a1[j], pk(__uint_as_float(ab[2 * j]), __uint_as_float(ab[2 * j + 1])));
+        t.a2[j] = fma2(d[j], d[j], t.a2[j]);
+    }
+    const int m0 = __vimax3_s32((int)ab[0], (int)ab[1], (int)ab[2]);
+    const int m1 = __vimax3_s32((int)ab[3], (int)ab[4], (int)ab[5]);
+    const int m2 = __vimax3_s32((int)ab[6], (int)ab[7], (int)mxb);
+    mxb = (uint32_t)__vimax3_s32(m0, m1, m2);
+}
 
 // x_hat of eight codes (biased fields u) -> bf16x8; with STATS the
 // differences against the source word xw are accumulated instead.
 template <bool STATS>
 __device__ __forceinline__ uint4 dq8(const uint32_t (&u)[8], const u64 (&cp)[4], const u64 (&sp)[4],
-                                    const uint4& xw, u64& a1, u64& a2, uint32_t& mxb) {
+                                    const uint4& xw, TileAcc& t, uint32_t& mxb) {
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -155,14 +180,10 @@ __device__ __forceinline__ uint4 dq8(const uint32_t (&u)[8], const u64 (&cp)[4],
     }
     if (STATS) {
         const uint32_t xs[4] = {xw.x, xw.y, xw.z, xw.w};
+        u64 d[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const u64 d = sub2(widen_bf16x2(xs[j]), widen_bf16x2(o[j]));
-            const uint32_t al = lo_bits(d) & 0x7FFFFFFFu, ah = hi_bits(d) & 0x7FFFFFFFu;
-            a1 = add2(a1, pk(__uint_as_float(al), __uint_as_float(ah)));
-            a2 = fma2(d, d, a2);
-            mxb = (uint32_t)__vimax3_s32((int)mxb, (int)al, (int)ah);
-        }
+        for (int j = 0; j < 4; ++j) d[j] = sub2(widen_bf16x2(xs[j]), widen_bf16x2(o[j]));
+        acc8(d, t, mxb);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -171,7 +192,7 @@ __device__ __forceinline__ uint4 dq8(const uint32_t (&u)[8], const u64 (&cp)[4],
 // form: q = field - off, then ((float)q - zp) * s exactly as the reference
 template <bool STATS>
 __device__ __forceinline__ uint4 dq8_slow(const uint32_t (&u)[8], int off, const float (&zp)[8], const float (&s)[8],
-                                         const uint4& xw, u64& a1, u64& a2, uint32_t& mxb) {
+                                         const uint4& xw, TileAcc& t, uint32_t& mxb) {
     float v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -187,29 +208,35 @@ __device__ __forceinline__ uint4 dq8_slow(const uint32_t (&u)[8], int off, const
     out.w = pack_bf16x2(v[6], v[7]);
     if (STATS) {
         const uint32_t xs[4] = {xw.x, xw.y, xw.z, xw.w}, os[4] = {out.x, out.y, out.z, out.w};
+        u64 d[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const u64 d = sub2(widen_bf16x2(xs[j]), widen_bf16x2(os[j]));
-            const uint32_t al = lo_bits(d) & 0x7FFFFFFFu, ah = hi_bits(d) & 0x7FFFFFFFu;
-            a1 = add2(a1, pk(__uint_as_float(al), __uint_as_float(ah)));
-            a2 = fma2(d, d, a2);
-            mxb = (uint32_t)__vimax3_s32((int)mxb, (int)al, (int)ah);
-        }
+        for (int j = 0; j < 4; ++j) d[j] = sub2(widen_bf16x2(xs[j]), widen_bf16x2(os[j]));
+        acc8(d, t, mxb);
     }
     return out;
+}
+
+// A thread's statistics, reduced over its warp in float32 (a fixed shuffle
+// tree: 5 roundings, ~3e-7 relative, far inside the 1e-5 bar) and widened to
+// double; the max is exact.  Lane 0 holds the warp's values.
+__device__ __forceinline__ void warp_partial(const Acc2& A, double& s1, double& s2, double& mx) {
+    float f1 = __fsub_rn(A.s1, A.e1), f2 = __fsub_rn(A.s2, A.e2), fm = __uint_as_float(A.mxb);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        f1 = __fadd_rn(f1, __shfl_xor_sync(0xFFFFFFFFu, f1, o));
+        f2 = __fadd_rn(f2, __shfl_xor_sync(0xFFFFFFFFu, f2, o));
+        fm = fmaxf(fm, __shfl_xor_sync(0xFFFFFFFFu, fm, o));
+    }
+    s1 = (double)f1;
+    s2 = (double)f2;
+    mx = (double)fm;
 }
 
 __device__ __forceinline__ void block_reduce_partial(const Acc2& A, Partial* partials)
 {
     __shared__ double sh1[kThr / 32], sh2[kThr / 32], shm[kThr / 32];
-    double s1 = (double)A.s1 - (double)A.e1;
-    double s2 = (double)A.s2 - (double)A.e2;
-    double mx = (double)__uint_as_float(A.mxb);
-    for (int o = 16; o > 0; o >>= 1) {
-        s1 += __shfl_xor_sync(0xFFFFFFFFu, s1, o);
-        s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, o);
-        mx = fmax(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    }
+    double s1, s2, mx;
+    warp_partial(A, s1, s2, mx);
     const int w = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) { sh1[w] = s1; sh2[w] = s2; shm[w] = mx; }
     __syncthreads();

@@ -888,14 +888,23 @@ ds_kernel(const QArgs a, int lcpr, int lg, Partial* partials, unsigned int* done
                         if (ASYM) fast_t = fast_t && fmaxf(fabsf(z0), fabsf(z1)) < 0x1p21f;
                     }
                 }
-                u64 a1 = 0, a2 = 0;
+                // groups along C: every row's scale and zero point, all loads issued together
+                float ssr[RPT], zsr[RPT];
+                if (!ALONG_T) {
+#pragma unroll
+                    for (int j = 0; j < RPT; ++j) {
+                        const int64_t mi = ((int64_t)o * Tq + t0 + j) * gpr + (int64_t)(cofs >> lg);
+                        ssr[j] = ld_meta<SDT>(a.scale, mi);
+                        zsr[j] = ASYM ? ld_meta<ZDT>(a.zero, mi) : 0.0f;
+                    }
+                }
+                TileAcc ta;
 #pragma unroll
                 for (int j = 0; j < RPT; ++j) {
                     float zs = 0.0f, ss = 1.0f;
                     if (!ALONG_T) {
-                        const int64_t mi = ((int64_t)o * Tq + t0 + j) * gpr + (int64_t)(cofs >> lg);
-                        ss = ld_meta<SDT>(a.scale, mi);
-                        zs = ASYM ? ld_meta<ZDT>(a.zero, mi) : 0.0f;
+                        ss = ssr[j];
+                        zs = zsr[j];
                         u64 c1, s1;
                         dq_pair_consts(ss, zs, off, c1, s1);
                         cp[0] = cp[1] = cp[2] = cp[3] = c1;
@@ -906,7 +915,7 @@ ds_kernel(const QArgs a, int lcpr, int lg, Partial* partials, unsigned int* done
                     const bool fast = ALONG_T ? fast_t : (!ASYM || fabsf(zs) < 0x1p21f);
                     uint4 ow;
                     if (fast) {
-                        ow = dq8<STATS>(u, cp, sp, xw[j], a1, a2, A.mxb);
+                        ow = dq8<STATS>(u, cp, sp, xw[j], ta, A.mxb);
                     } else {
                         // exact reference order for groups with a very large zero point
                         float sf[8], zf[8];
@@ -917,11 +926,11 @@ ds_kernel(const QArgs a, int lcpr, int lg, Partial* partials, unsigned int* done
                             sf[k] = ld_meta<SDT>(a.scale, ALONG_T ? mi + k : mi);
                             zf[k] = ASYM ? ld_meta<ZDT>(a.zero, ALONG_T ? mi + k : mi) : 0.0f;
                         }
-                        ow = dq8_slow<STATS>(u, off, zf, sf, xw[j], a1, a2, A.mxb);
+                        ow = dq8_slow<STATS>(u, off, zf, sf, xw[j], ta, A.mxb);
                     }
                     if (!STATS) optr[j * vstride] = ow;
                 }
-                if (STATS) A.fold(a1, a2);
+                if (STATS) A.fold(ta);
             } else {
                 // tail: the last partial row block and the residual window
                 for (int j = 0; j < RPT; ++j) {
@@ -946,9 +955,9 @@ ds_kernel(const QArgs a, int lcpr, int lg, Partial* partials, unsigned int* done
                     }
                     uint32_t u[8];
                     unpack_biased8<BITS>(q.is_signed ? flip_signs<BITS>(w) : w, u);
-                    u64 a1 = 0, a2 = 0;
-                    const uint4 ow = dq8_slow<STATS>(u, off, zf, sf, xv, a1, a2, A.mxb);
-                    if (STATS) A.fold(a1, a2);
+                    TileAcc ta;
+                    const uint4 ow = dq8_slow<STATS>(u, off, zf, sf, xv, ta, A.mxb);
+                    if (STATS) A.fold(ta);
                     else *reinterpret_cast<uint4*>(out + xo) = ow;
                 }
             }
@@ -1104,25 +1113,40 @@ wds_t_kernel(const QArgs a, Partial* partials, unsigned int* done, kvq_err* out_
         const unsigned char* cbase = st + L::offCodes + (uint32_t)(chan0 / 8) * BITS;
         const unsigned char* xbase = st + chan0 * 2;
         __nv_bfloat16* obase = out + ((uint64_t)o * T32 + row0) * C + chan0;
-        u64 a1 = 0, a2 = 0;
-        auto row = [&](int r) {
-            W cw = *reinterpret_cast<const W*>(cbase + (uint32_t)r * L::kCodeRowB);
+        TileAcc ta;
+        auto row_from = [&](int r, W cw, const uint4& xw) {
             uint32_t u[8];
             unpack_biased8<BITS>(q.is_signed ? flip_signs<BITS>(cw) : cw, u);
-            const uint4 xw = STATS ? *reinterpret_cast<const uint4*>(xbase + (uint32_t)r * 256u) : make_uint4(0, 0, 0, 0);
             uint4 ow;
-            if (fast) ow = dq8<STATS>(u, cp, sp, xw, a1, a2, A.mxb);
-            else ow = dq8_slow<STATS>(u, off, zf, sf, xw, a1, a2, A.mxb);
+            if (fast) ow = dq8<STATS>(u, cp, sp, xw, ta, A.mxb);
+            else ow = dq8_slow<STATS>(u, off, zf, sf, xw, ta, A.mxb);
             if (!STATS) *reinterpret_cast<uint4*>(obase + (uint64_t)r * C) = ow;
         };
-        if (nrows == CR) {
+        auto row = [&](int r) {
+            const W cw = *reinterpret_cast<const W*>(cbase + (uint32_t)r * L::kCodeRowB);
+            const uint4 xw = STATS ? *reinterpret_cast<const uint4*>(xbase + (uint32_t)r * 256u) : make_uint4(0, 0, 0, 0);
+            row_from(r, cw, xw);
+        };
+        if (nrows == CR && STATS) {
+            // a whole tile: every shared-memory load of the lane's rows first
+            constexpr int NR = CR / RSTEP;
+            W cws[NR];
+            uint4 xws[NR];
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                cws[i] = *reinterpret_cast<const W*>(cbase + (uint32_t)(rq + RSTEP * i) * L::kCodeRowB);
+                xws[i] = *reinterpret_cast<const uint4*>(xbase + (uint32_t)(rq + RSTEP * i) * 256u);
+            }
+#pragma unroll
+            for (int i = 0; i < NR; ++i) row_from(rq + RSTEP * i, cws[i], xws[i]);
+        } else if (nrows == CR) {
 #pragma unroll 4
             for (int i = 0; i < CR / RSTEP; ++i) row(rq + RSTEP * i);
         } else {
             for (int i = 0; i < CR / RSTEP; ++i)
                 if (rq + RSTEP * i < nrows) row(rq + RSTEP * i);
         }
-        if (STATS) A.fold(a1, a2);
+        if (STATS) A.fold(ta);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -1143,12 +1167,8 @@ wds_t_kernel(const QArgs a, Partial* partials, unsigned int* done, kvq_err* out_
     // ---- block partial over the consumer warps, then the fused final reduction
     __shared__ double w1[NCW], w2[NCW], wm[NCW];
     __shared__ bool s_last;
-    double d1 = (double)A.s1 - (double)A.e1, d2 = (double)A.s2 - (double)A.e2, dm = (double)__uint_as_float(A.mxb);
-    for (int o2 = 16; o2 > 0; o2 >>= 1) {
-        d1 += __shfl_xor_sync(0xFFFFFFFFu, d1, o2);
-        d2 += __shfl_xor_sync(0xFFFFFFFFu, d2, o2);
-        dm = fmax(dm, __shfl_xor_sync(0xFFFFFFFFu, dm, o2));
-    }
+    double d1, d2, dm;
+    warp_partial(A, d1, d2, dm);
     if (lane == 0) { w1[warp] = d1; w2[warp] = d2; wm[warp] = dm; }
     asm volatile("bar.sync 1, %0;" ::"r"(kCons) : "memory");
     if (threadIdx.x == 0) {
