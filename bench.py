@@ -293,6 +293,13 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
+    if args.only == "fullmodel":
+        # the full-model INT8 rows alone (profiling; --fullmodel-layers shrinks the case)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+        return {"metric": METRIC, "unit": UNIT, "n_gpus": 1, "data": "synthetic",
+                "config": {"workload": f"fullmodel_int8[L{args.fullmodel_layers},T8192,H32,d128]", "only": "fullmodel"},
+                "configs": run_configs(b, dev, stream, flush, only_fullmodel=True, layers=args.fullmodel_layers)}
     with torch.cuda.stream(stream):
         st = Step(b, dev, stream, args.only, rank)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -482,10 +489,11 @@ def quant_bytes(shape, x_es, cB, sB, zB, rB):
     return x + cB + sB + zB + rB, x + cB + sB + zB
 
 
-def run_configs(b, dev, stream, flush, runs=20):
+def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32):
     """Median over `runs` (L2 flushed before each) of every op of the large
     configurations: KIVI INT4 (2), full-model INT8 per channel (3), the
-    group / bit-width sweep (4), H2O / SnapKV (5); the tiny one (1) in us."""
+    group / bit-width sweep (4), H2O / SnapKV (5); the tiny one (1) in us.
+    only_fullmodel: the full-model rows alone, with `layers` layers."""
     import torch
     from kv_cache_quantization_kvq_gb300 import workloads as W
     peak, _ = measured_peak()
@@ -528,6 +536,10 @@ def run_configs(b, dev, stream, flush, runs=20):
             out[f"{tag}/{name}/bytes_per_number"] = round((cB + sB) / (shape[0] * shape[1] * shape[2]), 6)
             del qt, ws, outx
 
+    if only_fullmodel:
+        K, V = W.fullmodel_kv(dev, seed=3, layers=layers)
+        qdq(f"3_fullmodel_int8_L{layers}", [("K", K), ("V", V)], b.QParams.sym(8, axis=b.ALONG_T, group=0))
+        return out
     # 2: KIVI INT4
     K, V = W.kivi_kv(dev, seed=2)
     for axis, x, name in ((b.ALONG_T, K, "K"), (b.ALONG_C, V, "V")):
@@ -702,8 +714,11 @@ def main():
                          "branches of the step graph")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue the timed steps as plain C-ABI calls instead of replaying a captured CUDA graph")
-    ap.add_argument("--only", choices=("all", "kivi", "evict"), default="all",
-                    help="time only the KIVI phases or only the eviction phases (profiling)")
+    ap.add_argument("--only", choices=("all", "kivi", "evict", "fullmodel"), default="all",
+                    help="time only the KIVI phases or only the eviction phases (profiling); "
+                         "fullmodel: only the full-model INT8 rows of the per-configuration table")
+    ap.add_argument("--fullmodel-layers", type=int, default=32,
+                    help="layers of the full-model INT8 workload with --only fullmodel (a smaller profiling case)")
     ap.add_argument("--evict-tokens", type=int, default=None,
                     help="context length T of the eviction workload (profiling of a smaller case; "
                          "the timed workload keeps the default)")
