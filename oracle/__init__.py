@@ -72,9 +72,11 @@ def _load():
         lib.oracle_h2o_select.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp]
         lib.oracle_snapkv_select.argtypes = [vp, i64, i64, i64, i64, i64, i64, vp, vp]
         lib.oracle_compact.argtypes = [vp, i64, i64, i64, i64, vp, i64, vp]
+        lib.oracle_dequantize_f64.argtypes = [vp, vp, vp, vp, P, i32, vp]
+        lib.oracle_attend.argtypes = [vp, i64, vp, vp, i64, i64, i64, vp]
         for f in ("oracle_sizes", "oracle_token_compression_ratio", "oracle_quantize",
                   "oracle_dequantize", "oracle_error_stats", "oracle_h2o_select",
-                  "oracle_snapkv_select", "oracle_compact"):
+                  "oracle_snapkv_select", "oracle_compact", "oracle_dequantize_f64", "oracle_attend"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -217,6 +219,29 @@ def compact(kv: np.ndarray, keep: np.ndarray) -> np.ndarray:
     K = keep.shape[1]
     out = np.zeros((H, K, D), kv.dtype)
     _check(_load().oracle_compact(_ptr(kv), kv.itemsize, H, T, D, _ptr(keep), K, _ptr(out)), "compact")
+    return out
+
+
+def dequantize_f64(qt: Quantized, shape, qp: QParams, x_dtype: int) -> np.ndarray:
+    """The cache rows in binary64: s * (q - zp) for quantized tokens, the
+    residual rows (stored in x_dtype) widened."""
+    out = np.zeros(shape, np.float64)
+    p = qp.c(shape)
+    _check(_load().oracle_dequantize_f64(_ptr(qt.codes), _ptr(qt.scale), _ptr(qt.zero), _ptr(qt.resid),
+                                         ctypes.byref(p), x_dtype, _ptr(out)), "dequantize_f64")
+    return out
+
+
+def attend(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """q [outer, group, C], k / v [outer, T, C] (binary64) -> y [outer, group, C]."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    outer, group, C = q.shape
+    T = k.shape[1]
+    assert k.shape == (outer, T, C) and v.shape == (outer, T, C)
+    out = np.zeros((outer, group, C), np.float64)
+    _check(_load().oracle_attend(_ptr(q), group, _ptr(k), _ptr(v), outer, T, C, _ptr(out)), "attend")
     return out
 
 

@@ -26,7 +26,10 @@
  *        K per channel and V per token), §"4 bit 的实际压缩率由分组大小决定"
  *        (payload ceil(N*bits/8) bytes plus per-group bf16 scale and zero),
  *        §"带残差区的压缩预算，逐项加起来" (most recent tokens stay bf16),
- *        §"少存 token：合并，或淘汰" (eviction really frees the dropped K/V).
+ *        §"少存 token：合并，或淘汰" (eviction really frees the dropped K/V),
+ *        §"K 的误差会改变权重，V 的误差会改变内容" (logit_t = q^T k_t / sqrt(d),
+ *        y = sum_t a_t v_t with a = softmax of the logits), §"让 kernel 接住收益"
+ *        (the attention kernel reads the quantized cache and dequantizes it).
  *
  * Readings taken where the pages are silent (each one also listed in the
  * design notes):
@@ -49,7 +52,11 @@
  *    recent window is min(W, T) tokens, the heavy set has
  *    min(B - W', T - W') tokens, and W > B is rejected;
  *  - SnapKV's observation score is the float32 mean of the last obs_window
- *    history rows (sequential sum, then one division).
+ *    history rows (sequential sum, then one division);
+ *  - decode attention over a quantized cache takes its rows in full precision,
+ *    s * (q - zp) in binary64 with the stored s and zp (a fused kernel rounds
+ *    nothing to the cache dtype in between), the residual rows as stored, and
+ *    computes the softmax attention itself in binary64.
  */
 #include <math.h>
 #include <stddef.h>
@@ -552,5 +559,76 @@ int oracle_compact(const void* kv, int64_t elem_size, int64_t heads, int64_t T, 
             if (i < 0 || i >= T) return OR_EINVAL;
             memcpy((char*)out + (size_t)(h * K + j) * row, (const char*)kv + (size_t)(h * T + i) * row, row);
         }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* decode attention over the dequantized cache                          */
+/* ------------------------------------------------------------------ */
+
+/* The cache rows in binary64: s * (q - zp) with the stored scale and zero
+ * point for the quantized tokens (exact: the difference of two small integers
+ * times a 24-bit scale fits 53 bits), the residual rows widened from the
+ * source dtype x_dtype.  out is [outer, T, C]. */
+int oracle_dequantize_f64(const void* codes, const void* scale, const void* zero, const void* resid,
+                          const or_params* p, int x_dtype, double* out)
+{
+    if (check_params(p, x_dtype) != OR_OK) return OR_EINVAL;
+    int64_t ng = group_count(p);
+    for (int64_t gidx = 0; gidx < ng; ++gidx) {
+        or_group G;
+        group_at(p, gidx, &G);
+        for (int64_t m = 0; m < G.count; ++m) {
+            int64_t xi = G.first + m * G.stride;
+            int32_t q = get_code((const uint8_t*)codes, p->bits, code_index(p, xi), codes_signed(p));
+            double s_use = (double)load_meta(scale, p->scale_dtype, G.meta);
+            double zp_use = p->mode == OR_ASYM ? (double)load_meta(zero, p->zero_dtype, G.meta) : 0.0;
+            out[xi] = s_use * ((double)q - zp_use);
+        }
+    }
+    int64_t Tq = quantized_tokens(p);
+    int64_t R = p->T - Tq;
+    for (int64_t o = 0; o < p->outer; ++o)
+        for (int64_t r = 0; r < R; ++r)
+            for (int64_t c = 0; c < p->C; ++c)
+                out[(o * p->T + Tq + r) * p->C + c] = load_as_double(resid, x_dtype, (o * R + r) * p->C + c);
+    return OR_OK;
+}
+
+/* y[o][j][:] = sum_t softmax_t( q[o][j][:] . k[o][t][:] / sqrt(C) ) v[o][t][:]
+ * in binary64; query head j of slice o reads KV slice o (group query heads
+ * per KV slice).  q, out: [outer][group][C]; k, v: [outer][T][C]. */
+int oracle_attend(const double* q, int64_t group, const double* k, const double* v, int64_t outer,
+                  int64_t T, int64_t C, double* out)
+{
+    if (outer < 0 || T < 1 || C < 1 || group < 1) return OR_EINVAL;
+    double* logit = (double*)malloc((size_t)T * sizeof(double));
+    if (!logit) return OR_EINVAL;
+    const double inv_sqrt = 1.0 / sqrt((double)C);
+    for (int64_t o = 0; o < outer; ++o)
+        for (int64_t j = 0; j < group; ++j) {
+            const double* qv = q + (o * group + j) * C;
+            double mx = -INFINITY;
+            for (int64_t t = 0; t < T; ++t) {
+                const double* kt = k + (o * T + t) * C;
+                double dot = 0.0;
+                for (int64_t c = 0; c < C; ++c) dot += qv[c] * kt[c];
+                logit[t] = dot * inv_sqrt;
+                if (logit[t] > mx) mx = logit[t];
+            }
+            double z = 0.0;
+            for (int64_t t = 0; t < T; ++t) {
+                logit[t] = exp(logit[t] - mx);
+                z += logit[t];
+            }
+            double* y = out + (o * group + j) * C;
+            for (int64_t c = 0; c < C; ++c) y[c] = 0.0;
+            for (int64_t t = 0; t < T; ++t) {
+                const double* vt = v + (o * T + t) * C;
+                for (int64_t c = 0; c < C; ++c) y[c] += logit[t] * vt[c];
+            }
+            for (int64_t c = 0; c < C; ++c) y[c] /= z;
+        }
+    free(logit);
     return OR_OK;
 }

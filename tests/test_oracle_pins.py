@@ -625,3 +625,90 @@ def test_compact_is_row_gather():
         assert np.array_equal(out[h], kv[h][keep[h]])
     with pytest.raises(O.OracleError):
         O.compact(kv, np.full((3, 2), 50, np.int32))
+
+
+# ---------------------------------------------------------------- decode attention over the cache
+# "KV cache 压缩：把历史装得更小" §"K 的误差会改变权重，V 的误差会改变内容":
+# logit_t = q^T k_t / sqrt(d), y = sum_t a_t v_t with a = softmax(logits).
+
+
+def test_attend_zero_query_is_the_mean_of_v():
+    """q = 0 makes every logit 0: uniform weights, y = mean of the value rows
+    (catches an unnormalised sum or a dropped row)."""
+    rng = np.random.default_rng(40)
+    k, v = rng.standard_normal((2, 2, 37, 16))
+    y = O.attend(np.zeros((2, 3, 16)), k, v)
+    for j in range(3):
+        assert np.allclose(y[:, j], v.mean(axis=1), rtol=1e-13, atol=1e-15)
+
+
+def test_attend_single_token_returns_its_value():
+    rng = np.random.default_rng(41)
+    q, k, v = rng.standard_normal((3, 4, 1, 8))
+    assert np.allclose(O.attend(q, k, v)[:, 0], v[:, 0], rtol=1e-14, atol=0)
+
+
+def test_attend_two_keys_sigmoid_closed_form():
+    """Two keys: a_0 = 1 / (1 + exp(-(q.k0 - q.k1) / sqrt(d))) (catches a wrong
+    temperature -- 1/d, no scaling -- or a transposed contraction)."""
+    d = 64
+    rng = np.random.default_rng(42)
+    for _ in range(5):
+        q = rng.standard_normal(d)
+        k = rng.standard_normal((2, d))
+        v = rng.standard_normal((2, d))
+        a0 = 1.0 / (1.0 + math.exp(-(q @ k[0] - q @ k[1]) / math.sqrt(d)))
+        want = a0 * v[0] + (1 - a0) * v[1]
+        got = O.attend(q.reshape(1, 1, d), k.reshape(1, 2, d), v.reshape(1, 2, d))[0, 0]
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-14)
+
+
+def test_attend_is_invariant_to_a_common_key_shift():
+    """Adding one vector u to every key adds q.u / sqrt(d) to every logit, which
+    the softmax cancels (catches a missing max subtraction that overflows, or
+    weights not normalised per query)."""
+    rng = np.random.default_rng(43)
+    q = rng.standard_normal((2, 2, 32)) * 3
+    k, v = rng.standard_normal((2, 2, 50, 32))
+    u = rng.standard_normal(32) * 2000      # shifted logits near +-4000: exp overflows binary64 unless the max is taken out
+    assert np.allclose(O.attend(q, k, v), O.attend(q, k + u, v), rtol=1e-9, atol=1e-11)
+
+
+def test_attend_error_bounds_of_the_pages():
+    """The pages' bounds: |delta logit_t| <= ||q|| ||delta k_t|| / sqrt(d), with
+    equality when delta k_t is parallel to q (read off the two-key weights), and,
+    for fixed weights, ||delta y|| <= max_t ||delta v_t||."""
+    d = 32
+    rng = np.random.default_rng(44)
+    for _ in range(10):
+        q = rng.standard_normal(d)
+        k = rng.standard_normal((2, d))
+        v = np.zeros((2, d))
+        v[0, 0] = 1.0                        # y[0] = a_0: the two-key weight
+        dk = q * rng.uniform(0.01, 0.3)      # delta k_0 parallel to q
+        a = O.attend(q.reshape(1, 1, d), k.reshape(1, 2, d), v.reshape(1, 2, d))[0, 0, 0]
+        b = O.attend(q.reshape(1, 1, d), (k + [dk, 0 * dk]).reshape(1, 2, d), v.reshape(1, 2, d))[0, 0, 0]
+        dlogit = math.log(b / (1 - b)) - math.log(a / (1 - a))
+        assert dlogit == pytest.approx(np.linalg.norm(q) * np.linalg.norm(dk) / math.sqrt(d), rel=1e-9)
+    q = rng.standard_normal((1, 4, d))
+    k, v = rng.standard_normal((2, 1, 300, d))
+    dv = rng.standard_normal((1, 300, d)) * rng.uniform(0, 0.1, (1, 300, 1))
+    dy = O.attend(q, k, v + dv) - O.attend(q, k, v)
+    assert np.all(np.linalg.norm(dy, axis=-1) <= np.linalg.norm(dv, axis=-1).max() * (1 + 1e-12))
+
+
+def test_dequantize_f64_agrees_with_the_float32_dequantizer():
+    """The binary64 cache rows differ from the float32 dequantizer's x_hat by
+    at most its one rounding, and the residual rows are the stored ones."""
+    rng = np.random.default_rng(45)
+    x = bf16_bits((rng.standard_normal((2, 300, 128)) * 2).astype(np.float32)).reshape(2, 300, 128)
+    for qp in (O.QParams.asym(4, 0, 15, axis=O.ALONG_T, group=64, residual=44, scale_dtype=O.BF16, zero_dtype=O.BF16),
+               O.QParams.asym(4, 0, 15, axis=O.ALONG_C, group=64, residual=44, scale_dtype=O.BF16, zero_dtype=O.BF16),
+               O.QParams.sym(8, axis=O.ALONG_T, group=0, residual=0),
+               O.QParams.sym(2, axis=O.ALONG_C, group=32, residual=3, scale_dtype=O.BF16)):
+        qt = O.quantize(x, O.BF16, qp)
+        x64 = O.dequantize_f64(qt, x.shape, qp, O.BF16)
+        x32 = O.dequantize(qt, x.shape, qp, O.F32).astype(np.float64)   # its residual rows need f32 input
+        Tq = 300 - qp.residual
+        assert np.all(np.abs(x64[:, :Tq] - x32[:, :Tq]) <= np.abs(x64[:, :Tq]) * 2.0 ** -24)
+        assert np.array_equal(x64[:, Tq:], O.bf16_bits_to_f32(x[:, Tq:]).astype(np.float64))
