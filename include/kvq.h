@@ -200,6 +200,39 @@ KVQ_API kvq_status kv_compact_kv(const void* k, const void* v, kvq_dtype dtype, 
                                  int64_t D, const int32_t* keep, int64_t K, void* out_k, void* out_v,
                                  void* stream);
 
+/* Decode attention over a quantized KV cache, with the dequantization fused
+ * into the attention kernel.  [KVC] §"量化：位置都留着，每个数更短": the
+ * attention kernel reads the low-bit cache and dequantizes it; §"让 kernel 接住
+ * 收益": only a fused dequantization turns the smaller cache into fewer bytes
+ * moved; §"K 的误差会改变权重，V 的误差会改变内容": logit_t = q^T k_t / sqrt(d)
+ * and y = sum_t a_t v_t with a = softmax(logits).
+ *
+ * For every KV slice o of the cache (outer = batch * kv_heads) and each of its
+ * `group` query heads j (grouped-query attention: query head o*group + j reads
+ * KV slice o), with C = head_dim:
+ *     y[o][j][:] = sum_t softmax_t( q[o][j][:] . k[o][t][:] / sqrt(C) ) v[o][t][:],
+ * over all T tokens, where k and v are the cache rows: s * (code - zero_point)
+ * for the quantized tokens t < Tq, in full float precision (nothing is rounded
+ * to the cache dtype in between), and the bf16 residual rows for t >= Tq.
+ *  - q: [outer][group][C] float32 (device); out: [outer][group][C] float32.
+ *  - K: the buffers kvq_quantize wrote for a bf16 key cache of `shape` with
+ *    k_params (groups along T, the group a multiple of 32 tokens); V likewise
+ *    with v_params (groups along C of 32, 64 or 128 channels).  Both formats
+ *    need the same bit width and the same residual length.  Zero-point
+ *    pointers are ignored for symmetric formats.
+ *  - shape: the caches' [outer, T, C]; supported: C = 128, group 1 .. 8.
+ *  - workspace: at least kvq_attend_workspace(shape, group) bytes (the
+ *    partial results of the splits of T); no initialisation needed.
+ *  - Errors: KVQ_EINVAL (NULL or misaligned buffers, bad shape or group,
+ *    formats inconsistent with each other), KVQ_EUNSUPPORTED (a valid
+ *    format this kernel does not cover), KVQ_EWORKSPACE. */
+KVQ_API kvq_status kvq_attend_workspace(const kvq_shape* shape, int64_t group, size_t* workspace_B);
+KVQ_API kvq_status kvq_attend_decode(const float* q, int64_t group, const void* k_codes, const void* k_scale,
+                                     const void* k_zero, const void* k_resid, const kvq_qparams* k_params,
+                                     const void* v_codes, const void* v_scale, const void* v_zero,
+                                     const void* v_resid, const kvq_qparams* v_params, const kvq_shape* shape,
+                                     float* out, void* workspace, size_t workspace_B, void* stream);
+
 /* Size of the library's fixed scratch array used by kvq_error_stats_noalloc. */
 #define KVQ_NOALLOC_SCRATCH_BYTES (1 << 20)
 

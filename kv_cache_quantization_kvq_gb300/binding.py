@@ -66,6 +66,8 @@ def _load() -> ctypes.CDLL:
         "kv_compact": [vp, i32, i64, i64, i64, vp, i64, vp, vp],
         "kv_compact_kv": [vp, vp, i32, i64, i64, i64, vp, i64, vp, vp, vp],
         "kvq_error_stats_noalloc": [vp, i32, vp, vp, vp, vp, S, P, vp, vp],
+        "kvq_attend_workspace": [S, i64, psz],
+        "kvq_attend_decode": [vp, i64, vp, vp, vp, vp, P, vp, vp, vp, vp, P, S, vp, vp, sz, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -84,7 +86,7 @@ LIB = _load()
 EXPORTS = ("kvq_quantized_sizes", "kvq_quantize", "kvq_dequantize", "kvq_error_stats",
            "kvq_compression_ratio", "kvq_token_compression_ratio", "kv_select_workspace",
            "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kv_compact_kv", "kvq_last_error", "kvq_version",
-           "kvq_error_stats_noalloc")
+           "kvq_error_stats_noalloc", "kvq_attend_workspace", "kvq_attend_decode")
 
 # size of the library's fixed scratch array behind kvq_error_stats_noalloc
 NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -222,6 +224,21 @@ def kv_compact_kv(k, v, dtype, heads, T, D, keep, K, out_k, out_v, stream=None):
                              _stream(stream)))
 
 
+def kvq_attend_workspace(shape, group: int) -> int:
+    s, n = _shape(shape), ctypes.c_size_t()
+    _check(LIB.kvq_attend_workspace(ctypes.byref(s), int(group), ctypes.byref(n)))
+    return n.value
+
+
+def kvq_attend_decode(q, group, k_codes, k_scale, k_zero, k_resid, kqp: QParams, v_codes, v_scale, v_zero,
+                      v_resid, vqp: QParams, shape, out, workspace, workspace_B, stream=None):
+    s, pk, pv = _shape(shape), kqp.c(), vqp.c()
+    _check(LIB.kvq_attend_decode(_ptr(q), int(group), _ptr(k_codes), _ptr(k_scale), _ptr(k_zero), _ptr(k_resid),
+                                 ctypes.byref(pk), _ptr(v_codes), _ptr(v_scale), _ptr(v_zero), _ptr(v_resid),
+                                 ctypes.byref(pv), ctypes.byref(s), _ptr(out), _ptr(workspace), int(workspace_B),
+                                 _stream(stream)))
+
+
 def kvq_last_error() -> str:
     return LIB.kvq_last_error().decode(errors="replace")
 
@@ -342,4 +359,19 @@ def compact(kv, keep, out=None, stream=None):
     if out is None:
         out = torch.empty((H, K, D), dtype=kv.dtype, device=kv.device)
     kv_compact(kv, code, H, T, D, keep, K, out, stream)
+    return out
+
+
+def attend_decode(q, qk: Quantized, qv: Quantized, out=None, workspace=None, stream=None):
+    """q: CUDA float32 [outer, group, C]; qk / qv: the quantized key and value
+    caches of one bf16 [outer, T, C] shape -> float32 [outer, group, C], the
+    attention output over the cache with the dequantization fused in."""
+    import torch
+    outer, group, C = q.shape
+    if out is None:
+        out = torch.empty((outer, group, C), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = _empty(kvq_attend_workspace(qk.shape, group), q.device)
+    kvq_attend_decode(q, group, qk.codes, qk.scale, qk.zero, qk.resid, qk.qp, qv.codes, qv.scale, qv.zero,
+                      qv.resid, qv.qp, qk.shape, out, workspace, workspace.numel(), stream)
     return out

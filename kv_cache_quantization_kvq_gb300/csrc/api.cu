@@ -284,6 +284,71 @@ kvq_status kvq_error_stats(const void* x, kvq_dtype x_dtype, const void* codes, 
     return cuda_status(kvq::launch_error_stats(a, out_dev, (cudaStream_t)stream), "kvq_error_stats launch");
 }
 
+kvq_status kvq_attend_workspace(const kvq_shape* shape, int64_t group, size_t* workspace_B)
+{
+    if (!shape || !workspace_B) return fail(KVQ_EINVAL, "shape and workspace_B must not be NULL");
+    if (shape->outer < 0 || shape->T < 0 || shape->C < 0 || group < 1) return fail(KVQ_EINVAL, "negative extent or group < 1");
+    if (!mul_ok(shape->outer, group, std::max<int64_t>(shape->T, 1))) return fail(KVQ_EINVAL, "tensor too large");
+    *workspace_B = kvq::attend_workspace(shape->outer, shape->T, group);
+    return KVQ_OK;
+}
+
+kvq_status kvq_attend_decode(const float* q, int64_t group, const void* k_codes, const void* k_scale,
+                             const void* k_zero, const void* k_resid, const kvq_qparams* k_params,
+                             const void* v_codes, const void* v_scale, const void* v_zero, const void* v_resid,
+                             const kvq_qparams* v_params, const kvq_shape* shape, float* out, void* workspace,
+                             size_t workspace_B, void* stream)
+{
+    kvq::AttendArgs a;
+    kvq_status s = make_spec(shape, KVQ_BF16, k_params, a.k);
+    if (s != KVQ_OK) return s;
+    if ((s = make_spec(shape, KVQ_BF16, v_params, a.v)) != KVQ_OK) return s;
+    if (shape->T == 0) return fail(KVQ_EINVAL, "attention over an empty cache is undefined (T = 0)");
+    if (group < 1) return fail(KVQ_EINVAL, "group must be >= 1 (got %lld)", (long long)group);
+    if (a.k.R != a.v.R) return fail(KVQ_EINVAL, "K and V must keep the same residual window");
+    if (shape->C != 128) return fail(KVQ_EUNSUPPORTED, "fused attention supports head_dim 128 (got %lld)", (long long)shape->C);
+    if (group != 1 && group != 2 && group != 4 && group != 8)
+        return fail(KVQ_EUNSUPPORTED, "fused attention supports 1, 2, 4 or 8 query heads per KV head (got %lld)", (long long)group);
+    if (a.k.axis != KVQ_GROUP_ALONG_T || a.v.axis != KVQ_GROUP_ALONG_C)
+        return fail(KVQ_EUNSUPPORTED, "fused attention needs K grouped along T (per channel) and V along C (per token)");
+    if (a.k.bits != a.v.bits) return fail(KVQ_EUNSUPPORTED, "fused attention needs K and V of the same bit width");
+    if (a.k.Tq > 0 && a.k.ngroups > 1 && a.k.g % 32 != 0)
+        return fail(KVQ_EUNSUPPORTED, "fused attention needs K groups of a multiple of 32 tokens (got %lld)", (long long)a.k.g);
+    if (a.v.g != 32 && a.v.g != 64 && a.v.g != 128)
+        return fail(KVQ_EUNSUPPORTED, "fused attention needs V groups of 32, 64 or 128 channels (got %lld)", (long long)a.v.g);
+    const Sizes zk = sizes_of(a.k), zv = sizes_of(a.v);
+    const size_t qB = (size_t)(shape->outer * group * shape->C) * 4;
+    if ((s = need_ptr(q, qB, "q")) || (s = need_ptr(out, qB, "out")) ||
+        (s = need_ptr(k_codes, zk.codes, "k_codes")) || (s = need_ptr(k_scale, zk.scale, "k_scale")) ||
+        (s = need_ptr(k_zero, zk.zero, "k_zero")) || (s = need_ptr(k_resid, zk.resid, "k_resid")) ||
+        (s = need_ptr(v_codes, zv.codes, "v_codes")) || (s = need_ptr(v_scale, zv.scale, "v_scale")) ||
+        (s = need_ptr(v_zero, zv.zero, "v_zero")) || (s = need_ptr(v_resid, zv.resid, "v_resid")))
+        return s;
+    if ((s = need_align(q, 4, "q")) || (s = need_align(out, 4, "out")) || (s = need_align(k_codes, 16, "k_codes")) ||
+        (s = need_align(v_codes, 16, "v_codes")) || (s = need_align(k_resid, 16, "k_resid")) ||
+        (s = need_align(v_resid, 16, "v_resid")) || (s = need_align(k_scale, dtype_bytes(a.k.scale_dt), "k_scale")) ||
+        (s = need_align(v_scale, dtype_bytes(a.v.scale_dt), "v_scale")) ||
+        (s = need_align(k_zero, dtype_bytes(a.k.zero_dt), "k_zero")) ||
+        (s = need_align(v_zero, dtype_bytes(a.v.zero_dt), "v_zero")) || (s = need_align(workspace, 16, "workspace")))
+        return s;
+    const size_t need = kvq::attend_workspace(shape->outer, shape->T, group);
+    if (need && (!workspace || workspace_B < need))
+        return fail(KVQ_EWORKSPACE, "kvq_attend_decode needs %zu workspace bytes (got %zu)", need, workspace_B);
+    a.q = q;
+    a.group = group;
+    a.k_codes = k_codes;
+    a.k_scale = k_scale;
+    a.k_zero = a.k.mode == KVQ_ASYM ? k_zero : nullptr;
+    a.k_resid = k_resid;
+    a.v_codes = v_codes;
+    a.v_scale = v_scale;
+    a.v_zero = a.v.mode == KVQ_ASYM ? v_zero : nullptr;
+    a.v_resid = v_resid;
+    a.out = out;
+    a.ws = workspace;
+    return cuda_status(kvq::launch_attend(a, (cudaStream_t)stream), "kvq_attend_decode launch");
+}
+
 double kvq_compression_ratio(size_t orig_B, size_t codes_B, size_t scale_B, size_t zero_B, size_t resid_B)
 {
     const double d = (double)codes_B + (double)scale_B + (double)zero_B + (double)resid_B;

@@ -77,6 +77,20 @@ int64_t stream_stats_blocks(const QSpec& q, int sms);           // -1: not suppo
 // out_dev (done must be zero at launch and counts the finished blocks).
 cudaError_t stream_error_stats(const QArgs& a, void* partials, unsigned int* done, kvq_err* out_dev, cudaStream_t st);
 
+// ---- decode attention over a quantized cache (attend.cu)
+struct AttendArgs {
+    const float* q;                 // [outer][group][C]
+    int64_t group;                  // 1, 2, 4 or 8
+    const void *k_codes, *k_scale, *k_zero, *k_resid;
+    const void *v_codes, *v_scale, *v_zero, *v_resid;
+    QSpec k, v;                     // the two formats over the same [outer, T, C = 128]
+    float* out;                     // [outer][group][C]
+    void* ws;
+};
+int64_t attend_splits(int64_t T);
+size_t attend_workspace(int64_t outer, int64_t T, int64_t group);
+cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st);
+
 // ---- keep-set selection (select.cu) and compaction (compact.cu)
 struct SelectArgs {
     const float* hist;

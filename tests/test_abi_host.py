@@ -33,7 +33,7 @@ def declared_symbols():
 
 def test_library_exports_every_declared_symbol(kb):
     declared = declared_symbols()
-    assert len(declared) == 14
+    assert len(declared) == 16
     for name in declared:
         assert hasattr(kb.LIB, name), name
     assert declared == set(kb.EXPORTS)
@@ -198,3 +198,41 @@ def test_misaligned_buffers_rejected(kb):
         kb.kv_h2o_select(base, 2, 4, 64, 8, 2, base, None, base + 8, ws, 0)
     with pytest.raises(kb.KvqError):
         kb.kv_compact(base, kb.BF16, 2, 64, 8, base + 1, 4, base, 0)
+
+
+def test_attend_rejected_before_launch(kb):
+    """Fused decode attention: shape, group, format and buffer checks on the host."""
+    fake = 1 << 20  # never dereferenced: validation fails first
+    kq = kb.QParams.asym(4, 0, 15, axis=kb.ALONG_T, group=64, residual=128, scale_dtype=kb.BF16, zero_dtype=kb.BF16)
+    vq = kb.QParams.asym(4, 0, 15, axis=kb.ALONG_C, group=64, residual=128, scale_dtype=kb.BF16, zero_dtype=kb.BF16)
+    shape = (2, 1000, 128)
+    wB = kb.kvq_attend_workspace(shape, 2)
+    assert wB == 2 * 2 * 4 * (2 + 128) * 4           # outer x group x ceil(T/256) splits x (max, sum, C) floats
+    args = [fake] * 4
+
+    def call(q=fake, group=2, k=None, v=None, kp=kq, vp=vq, sh=shape, out=fake, ws=fake, wsB=wB):
+        kb.kvq_attend_decode(q, group, *(k or args), kp, *(v or args), vp, sh, out, ws, wsB, 0)
+
+    cases = [
+        (dict(q=None), kb.EINVAL),
+        (dict(out=None), kb.EINVAL),
+        (dict(group=0), kb.EINVAL),
+        (dict(sh=(2, 0, 128)), kb.EINVAL),
+        (dict(vp=kb.QParams.asym(4, 0, 15, axis=kb.ALONG_C, group=64, residual=5, scale_dtype=kb.BF16,
+                                 zero_dtype=kb.BF16)), kb.EINVAL),
+        (dict(k=[fake + 4, fake, fake, fake]), kb.EINVAL),               # codes not 16-byte aligned
+        (dict(sh=(2, 1000, 64)), kb.EUNSUPPORTED),
+        (dict(group=3), kb.EUNSUPPORTED),
+        (dict(kp=vq), kb.EUNSUPPORTED),                                  # K grouped per token
+        (dict(vp=kb.QParams.asym(8, 0, 255, axis=kb.ALONG_C, group=64, residual=128, scale_dtype=kb.BF16,
+                                 zero_dtype=kb.BF16)), kb.EUNSUPPORTED),  # bit widths differ
+        (dict(kp=kb.QParams.asym(4, 0, 15, axis=kb.ALONG_T, group=48, residual=128, scale_dtype=kb.BF16,
+                                 zero_dtype=kb.BF16)), kb.EUNSUPPORTED),  # K groups not a multiple of 32
+        (dict(ws=None), kb.EWORKSPACE),
+        (dict(wsB=wB - 1), kb.EWORKSPACE),
+    ]
+    for kw, status in cases:
+        with pytest.raises(kb.KvqError) as e:
+            call(**kw)
+        assert e.value.status == status, (kw, str(e.value))
+

@@ -1,0 +1,148 @@
+"""CUDA decode attention over a quantized cache (dequantization fused in) vs
+the CPU oracle.
+
+Both sides read the same quantized cache (the oracle's buffers, uploaded), so
+the comparison isolates the attention kernel.  The oracle computes in binary64
+("KV cache 压缩：把历史装得更小" §"K 的误差会改变权重，V 的误差会改变内容":
+logit_t = q.k_t / sqrt(d), y = sum_t softmax(logits)_t v_t, the cache rows as
+s * (q - zp) in full precision); the kernel computes in float32.
+
+Tolerance, derived from the kernel's float32 arithmetic (u = 2^-24,
+gamma_n = n u / (1 - n u), worst case, no probabilistic model):
+ - a base-2 logit is a sum of C products q_c * k_tc, each rounded once when
+   the K scale is folded into q, accumulated as two FMA chains of C/2 terms,
+   added, and scaled by the rounded log2(e)/sqrt(C):
+       |d l_t| <= gamma_{C/2+4} * log2(e)/sqrt(C) * sum_c |q_c k_tc|;
+ - a weight p_t = 2^(l_t - max) then carries a relative error of at most
+   ln2 * (2 max_t |d l_t| + u * spread) + 16 u (exp2f within 2 ulp, the
+   online-softmax rescalings and the merges of warps and splits);
+ - y = sum_t p_t v_t / sum_t p_t moves by at most twice that times
+   max_t |v_tc|, plus the accumulation of at most 64 tokens per warp, the
+   merges and the division: gamma_{72 + splits} * max_t |v_tc|.
+"""
+import math
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle as O
+from gpu_util import kb, kq_of
+from kv_cache_quantization_kvq_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+U = 2.0 ** -24
+
+
+def gamma(n):
+    return n * U / (1 - n * U)
+
+
+@pytest.fixture(scope="module")
+def b():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return kb()
+
+
+def upload(qt):
+    import torch
+    return [torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).ravel()).cuda() for a in
+            (qt.codes, qt.scale, qt.zero, qt.resid)]
+
+
+def bound(q, K, V, splits):
+    """Per-output tolerance (see the module docstring). q [O, G, C], K / V [O, T, C]."""
+    C = q.shape[-1]
+    S = np.einsum("ojc,otc->ojt", np.abs(q), np.abs(K))                 # sum_c |q_c k_tc|
+    dl = gamma(C / 2 + 4) * math.log2(math.e) / math.sqrt(C) * S.max(-1)
+    logit = np.einsum("ojc,otc->ojt", q, K) * math.log2(math.e) / math.sqrt(C)
+    spread = logit.max(-1) - logit.min(-1)
+    e_p = math.log(2) * (2 * dl + U * spread) + 16 * U
+    vmax = np.abs(V).max(axis=1)[:, None, :]                              # [O, 1, C]
+    return (2 * e_p[..., None] + gamma(72 + splits)) * vmax
+
+
+def run_case(b, shape, group, kq, vq, seed, kind="normal"):
+    import torch
+    outer, T, C = shape
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        xk = W.random_kv(rng, shape)
+        xv = W.random_kv(rng, shape)
+    else:                                   # "peaked": a few dominant keys
+        xk = (rng.standard_normal(shape) * 0.2).astype(np.float32)
+        xk[:, rng.integers(0, T, 3), :] *= 40.0
+        xv = rng.standard_normal(shape).astype(np.float32)
+    xk, xv = W.to_bf16_bits(xk), W.to_bf16_bits(xv)
+    q = rng.standard_normal((outer, group, C)).astype(np.float32)
+    qk, qv = O.quantize(xk, O.BF16, kq), O.quantize(xv, O.BF16, vq)
+    K = O.dequantize_f64(qk, shape, kq, O.BF16)
+    V = O.dequantize_f64(qv, shape, vq, O.BF16)
+    want = O.attend(q.astype(np.float64), K, V)
+
+    dk, dv = upload(qk), upload(qv)
+    qd = torch.from_numpy(q).cuda()
+    out = torch.full((outer, group, C), float("nan"), dtype=torch.float32, device="cuda")
+    wB = b.kvq_attend_workspace(shape, group)
+    ws = torch.empty(max(wB, 1), dtype=torch.uint8, device="cuda")
+    b.kvq_attend_decode(qd, group, *dk, kq_of(b, kq), *dv, kq_of(b, vq), shape, out, ws, wB)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    tol = bound(q.astype(np.float64), K, V, splits=-(-T // 256))
+    err = np.abs(got - want)
+    assert np.all(np.isfinite(got))
+    assert np.all(err <= tol), f"max err {err.max():.3e}, worst err/tol {(err / tol).max():.3f}"
+    return float(np.where(tol > 0, err / np.where(tol > 0, tol, 1), 0).max())
+
+
+KIVI_K = O.QParams.asym(4, 0, 15, axis=O.ALONG_T, group=64, residual=128, scale_dtype=O.BF16, zero_dtype=O.BF16)
+KIVI_V = O.QParams.asym(4, 0, 15, axis=O.ALONG_C, group=64, residual=128, scale_dtype=O.BF16, zero_dtype=O.BF16)
+
+CASES = [
+    # (outer, T), group, K format, V format
+    ((4, 1000), 1, KIVI_K, KIVI_V),
+    ((4, 1000), 2, KIVI_K, KIVI_V),
+    ((2, 1000), 4, KIVI_K, KIVI_V),
+    ((2, 1000), 8, KIVI_K, KIVI_V),
+    ((3, 777), 1, O.QParams.sym(8, axis=O.ALONG_T, group=32), O.QParams.sym(8, axis=O.ALONG_C, group=128)),
+    ((2, 300), 4, O.QParams.sym(2, axis=O.ALONG_T, group=0, residual=5, scale_dtype=O.BF16),
+     O.QParams.sym(2, axis=O.ALONG_C, group=32, residual=5, scale_dtype=O.BF16)),
+    ((2, 513), 2, O.QParams.asym(8, -128, 127, axis=O.ALONG_T, group=128, residual=17, zero_dtype=O.I8),
+     O.QParams.asym(8, -128, 127, axis=O.ALONG_C, group=64, residual=17, zero_dtype=O.I8)),
+    ((2, 150), 1, O.QParams.sym(4, axis=O.ALONG_T, group=64, residual=200),
+     O.QParams.sym(4, axis=O.ALONG_C, group=128, residual=200)),
+    ((3, 1), 8, O.QParams.sym(4, axis=O.ALONG_T, group=32), O.QParams.sym(4, axis=O.ALONG_C, group=32)),
+    ((1, 4100), 4, O.QParams.asym(4, -8, 7, axis=O.ALONG_T, group=96, residual=3, zero_dtype=O.F32),
+     O.QParams.asym(4, 0, 15, axis=O.ALONG_C, group=64, residual=3, zero_dtype=O.F32)),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=str)
+def test_attend_matches_oracle(b, case):
+    (outer, T), group, kq, vq = case
+    run_case(b, (outer, T, 128), group, kq, vq, zlib.crc32(repr(case).encode()))
+
+
+def test_attend_peaked_scores(b):
+    """A few keys 40x larger: nearly one-hot weights, large logit spread."""
+    run_case(b, (2, 2000, 128), 2, KIVI_K, KIVI_V, 7, kind="peaked")
+
+
+def test_attend_kivi_workload_full_size(b):
+    """The KIVI INT4 workload at full size (batch 8 x 8 KV heads, T 8192,
+    128-token residual), one query per KV head, every output checked."""
+    run_case(b, (64, 8192, 128), 1, KIVI_K, KIVI_V, 2)
+
+
+def test_attend_empty_outer(b):
+    import torch
+    shape = (0, 64, 128)
+    q = torch.zeros((0, 1, 128), dtype=torch.float32, device="cuda")
+    out = torch.zeros((0, 1, 128), dtype=torch.float32, device="cuda")
+    e = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    kq, vq = kq_of(b, KIVI_K), kq_of(b, KIVI_V)
+    b.kvq_attend_decode(q, 1, e, e, e, e, kq, e, e, e, e, vq, shape, out, e, 16)
+    torch.cuda.synchronize()
