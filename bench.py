@@ -293,6 +293,13 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
+    if args.only == "attend":
+        # the fused decode-attention rows alone (profiling)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+        return {"metric": METRIC, "unit": UNIT, "n_gpus": 1, "data": "synthetic",
+                "config": {"workload": "kivi_int4 decode attention [b8,h8,T8192,d128,g64,R128]", "only": "attend"},
+                "configs": run_configs(b, dev, stream, flush, only_attend=True)}
     if args.only == "fullmodel":
         # the full-model INT8 rows alone (profiling; --fullmodel-layers shrinks the case)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -489,11 +496,12 @@ def quant_bytes(shape, x_es, cB, sB, zB, rB):
     return x + cB + sB + zB + rB, x + cB + sB + zB
 
 
-def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32):
+def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32, only_attend=False):
     """Median over `runs` (L2 flushed before each) of every op of the large
     configurations: KIVI INT4 (2), full-model INT8 per channel (3), the
     group / bit-width sweep (4), H2O / SnapKV (5); the tiny one (1) in us.
-    only_fullmodel: the full-model rows alone, with `layers` layers."""
+    only_fullmodel: the full-model rows alone, with `layers` layers;
+    only_attend: the fused decode attention over the KIVI cache alone."""
     import torch
     from kv_cache_quantization_kvq_gb300 import workloads as W
     peak, _ = measured_peak()
@@ -542,10 +550,27 @@ def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32)
         return out
     # 2: KIVI INT4
     K, V = W.kivi_kv(dev, seed=2)
-    for axis, x, name in ((b.ALONG_T, K, "K"), (b.ALONG_C, V, "V")):
-        qp = b.QParams.asym(4, 0, 15, axis=axis, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
-        qdq("2_kivi_int4", [(name, x)], qp)
-    del K, V
+    if not only_attend:
+        for axis, x, name in ((b.ALONG_T, K, "K"), (b.ALONG_C, V, "V")):
+            qp = b.QParams.asym(4, 0, 15, axis=axis, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
+            qdq("2_kivi_int4", [(name, x)], qp)
+    # decode attention over the quantized KIVI cache (dequantization fused):
+    # bytes = the quantized K and V caches read + queries + outputs + split partials
+    kq = b.QParams.asym(4, 0, 15, axis=b.ALONG_T, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
+    vq = b.QParams.asym(4, 0, 15, axis=b.ALONG_C, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
+    qk, qv = b.quantize(K, kq, stream=stream), b.quantize(V, vq, stream=stream)
+    torch.cuda.synchronize()
+    cache_B = sum(t.numel() for t in (qk.codes, qk.scale, qk.zero, qk.resid, qv.codes, qv.scale, qv.zero, qv.resid))
+    outer = K.shape[0]
+    for G in (1, 4, 8):
+        q = torch.randn((outer, G, K.shape[2]), device=dev, generator=torch.Generator(device=dev).manual_seed(G))
+        o = torch.empty_like(q)
+        ws = torch.empty(b.kvq_attend_workspace(tuple(K.shape), G), dtype=torch.uint8, device=dev)
+        ms = med(lambda: b.attend_decode(q, qk, qv, out=o, workspace=ws, stream=stream))
+        out[f"2_kivi_int4/attend_decode_G{G}"] = entry(ms, cache_B + 2 * q.numel() * 4 + 2 * ws.numel())
+    del K, V, qk, qv
+    if only_attend:
+        return out
     # 3: full model INT8, per channel over all tokens
     K, V = W.fullmodel_kv(dev, seed=3)
     qdq("3_fullmodel_int8", [("K", K), ("V", V)], b.QParams.sym(8, axis=b.ALONG_T, group=0))
@@ -714,9 +739,10 @@ def main():
                          "branches of the step graph")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue the timed steps as plain C-ABI calls instead of replaying a captured CUDA graph")
-    ap.add_argument("--only", choices=("all", "kivi", "evict", "fullmodel"), default="all",
+    ap.add_argument("--only", choices=("all", "kivi", "evict", "fullmodel", "attend"), default="all",
                     help="time only the KIVI phases or only the eviction phases (profiling); "
-                         "fullmodel: only the full-model INT8 rows of the per-configuration table")
+                         "fullmodel / attend: only the full-model INT8 rows / the fused decode-attention "
+                         "rows of the per-configuration table")
     ap.add_argument("--fullmodel-layers", type=int, default=32,
                     help="layers of the full-model INT8 workload with --only fullmodel (a smaller profiling case)")
     ap.add_argument("--evict-tokens", type=int, default=None,

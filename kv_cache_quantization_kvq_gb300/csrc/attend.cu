@@ -18,9 +18,11 @@
 //    logit is sum_c A[j][c] * (code[c] - zp[c]) / sqrt(C), one FMA per code
 //    and query head;
 //  * online softmax in base 2 (running max and rescaled sums);
-//  * values, lane = 4 channels: the batch's V codes and per-token (scale,
-//    zero) are staged in shared memory, and every token adds
-//    (p_j * s) * (code - zeff) to the lane's channels.
+//  * values, half-warp = token, lane = 8 channels: the batch's V codes and
+//    per-token (scale, 2^23 + zeff) are staged in shared memory; each step
+//    takes two tokens (one per half-warp), a lane unpacks one packed code
+//    word of 8 channels and adds (p_j * s) * (code - zp); the halves are
+//    summed at the end.
 // The residual tokens (t >= Tq) are read as bf16 rows.  The CTA merges its
 // warps and writes (max, sum, unnormalised output) per query head; the merge
 // kernel combines the splits of T.
@@ -81,34 +83,13 @@ __device__ __forceinline__ typename CodeWord<BITS>::T word_at(const uint4* v, in
     }
 }
 
-// Four consecutive BITS-bit fields starting at field `c` of a packed row in
-// shared memory, as "2^23 + field" float bit patterns (offset binary when
-// signed: the caller subtracts 2^23 + zeff with zeff = off + zero point).
-template <int BITS>
-__device__ __forceinline__ void fields4(const unsigned char* row, int c, bool is_signed, uint32_t (&u)[4]) {
-    if constexpr (BITS == 4) {
-        uint32_t w = *reinterpret_cast<const uint16_t*>(row + c / 2);
-        if (is_signed) w ^= 0x8888u;
-        u[0] = kTwo23Bits | (w & 0xFu);
-        u[1] = kTwo23Bits | ((w >> 4) & 0xFu);
-        u[2] = kTwo23Bits | ((w >> 8) & 0xFu);
-        u[3] = kTwo23Bits | (w >> 12);
-    } else if constexpr (BITS == 8) {
-        uint32_t w = *reinterpret_cast<const uint32_t*>(row + c);
-        if (is_signed) w ^= 0x80808080u;
-        u[0] = __byte_perm(w, kTwo23Bits, 0x7440);
-        u[1] = __byte_perm(w, kTwo23Bits, 0x7441);
-        u[2] = __byte_perm(w, kTwo23Bits, 0x7442);
-        u[3] = __byte_perm(w, kTwo23Bits, 0x7443);
-    } else {
-        uint32_t w = row[c / 4];
-        if (is_signed) w ^= 0xAAu;
-        u[0] = kTwo23Bits | (w & 3u);
-        u[1] = kTwo23Bits | ((w >> 2) & 3u);
-        u[2] = kTwo23Bits | ((w >> 4) & 3u);
-        u[3] = kTwo23Bits | (w >> 6);
-    }
+// 16 bytes global -> shared without passing through registers (sm_80+).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gsrc) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -134,7 +115,7 @@ attend_split_kernel(const AttnArgs a)
     __shared__ __align__(16) float A[kAWarps][G][kAC];
     __shared__ __align__(16) float CZ[kAWarps][kAC];                 // 2^23 + zeff of the K group
     __shared__ __align__(16) unsigned char vst[kAWarps][32][kRowB];
-    __shared__ __align__(8) float2 vmeta[kAWarps][32][kAMaxVG];    // (scale, 2^23 + zeff)
+    __shared__ __align__(8) float2 vmeta[kAWarps][32][kAMaxVG];    // (scale, 2^23 + zeff) per token and V group
     __shared__ float wm[kAWarps][G], wl[kAWarps][G];
     float (*wo)[G][kAC] = A;
 
@@ -146,21 +127,33 @@ attend_split_kernel(const AttnArgs a)
     __syncthreads();
 
     float m[G], ell[G];
-    u64 acc_o[G][2];                             // lane's channels 4*lane .. 4*lane+3
+    u64 acc_o[G][4];                             // channels c8 .. c8+7 over this half-warp's tokens
 #pragma unroll
     for (int j = 0; j < G; ++j) {
         m[j] = -INFINITY;
         ell[j] = 0.0f;
-        acc_o[j][0] = acc_o[j][1] = 0;
+        acc_o[j][0] = acc_o[j][1] = acc_o[j][2] = acc_o[j][3] = 0;
     }
     int cur_gk = -1;
-    const int c4 = lane * 4;                     // this lane's first value channel
-    const int vgrp = c4 / a.gv;                  // its V group within a row
+    const int half = lane >> 4;                  // value side: which token of a step
+    const int c8 = (lane & 15) * 8;              // this lane's first value channel
+    const int vgrp = c8 / a.gv;                  // its V group within a row
 
     for (int b = 0; b < kATokWarp / 32; ++b) {
         const int64_t t0 = (int64_t)split * kAChunk + warp * kATokWarp + b * 32;
         if (t0 >= T) break;                      // warp-uniform
         const int64_t t = t0 + lane;
+
+        // ---- this batch's V codes: an asynchronous copy to shared memory, in
+        // flight while the scores are computed
+        const int64_t nq64 = Tq - t0;
+        const int nq = nq64 <= 0 ? 0 : (nq64 >= 32 ? 32 : (int)nq64);     // quantized tokens of the batch
+        if (nq > 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(a.vc + ((uint64_t)o * Tq + t0) * kRowB);
+            uint4* dst = reinterpret_cast<uint4*>(&vst[warp][0][0]);
+            for (int k = lane; k < nq * kNV; k += 32) cp_async16(dst + k, src + k);
+            cp_async_commit();
+        }
 
         // ---- K group constants folded into the queries (once per group)
         if (t0 < Tq) {
@@ -256,54 +249,53 @@ attend_split_kernel(const AttnArgs a)
             m[j] = mn;
             ell[j] = __fmaf_rn(ell[j], alpha, p[j]);
             const u64 al2 = pk(alpha, alpha);
-            acc_o[j][0] = mul2(acc_o[j][0], al2);
-            acc_o[j][1] = mul2(acc_o[j][1], al2);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc_o[j][k] = mul2(acc_o[j][k], al2);
         }
 
-        // ---- stage the batch's V codes and per-token constants
-        const int64_t nq64 = Tq - t0;
-        const int nq = nq64 <= 0 ? 0 : (nq64 >= 32 ? 32 : (int)nq64);     // quantized tokens of the batch
+        // ---- per-token V constants to shared memory; the staged codes have landed
         if (nq > 0) {
-            const uint4* src = reinterpret_cast<const uint4*>(a.vc + ((uint64_t)o * Tq + t0) * kRowB);
-            uint4* dst = reinterpret_cast<uint4*>(&vst[warp][0][0]);
-            for (int k = lane; k < nq * kNV; k += 32) dst[k] = __ldcs(src + k);
             if (lane < nq) {
                 for (int g = 0; g < a.ngv; ++g) {
                     const int64_t mi = (o * Tq + t) * a.ngv + g;
-                    const float s = load_meta(a.vs, a.vs_dt, mi);
-                    const float z = a.vz_dt == KVQ_NONE ? 0.0f : load_meta(a.vz, a.vz_dt, mi);
-                    vmeta[warp][lane][g] = make_float2(s, __fadd_rn(kTwo23, __fadd_rn((float)a.v_off, z)));
+                    const float sv = load_meta(a.vs, a.vs_dt, mi);
+                    const float zv = a.vz_dt == KVQ_NONE ? 0.0f : load_meta(a.vz, a.vz_dt, mi);
+                    vmeta[warp][lane][g] = make_float2(sv, __fadd_rn(kTwo23, __fadd_rn((float)a.v_off, zv)));
                 }
             }
+            cp_async_wait_all();
         }
         __syncwarp();
 
-        // ---- values, lane = 4 channels
+        // ---- values: step i takes token 2i + half, lane = 8 channels
         const int nt = T - t0 >= 32 ? 32 : (int)(T - t0);
-        for (int i = 0; i < nt; ++i) {
+        for (int i = 0; i < (nt + 1) / 2; ++i) {
+            const int ti = 2 * i + half;
             float pi[G];
 #pragma unroll
-            for (int j = 0; j < G; ++j) pi[j] = __shfl_sync(0xFFFFFFFFu, p[j], i);
-            if (i < nq) {
-                uint32_t u[4];
-                fields4<BITS>(&vst[warp][i][0], c4, a.v_signed, u);
-                const float2 sm = vmeta[warp][i][vgrp];
+            for (int j = 0; j < G; ++j) pi[j] = __shfl_sync(0xFFFFFFFFu, p[j], ti & 31);
+            if (ti < nq) {
+                W cw = *reinterpret_cast<const W*>(&vst[warp][ti][c8 * BITS / 8]);
+                uint32_t u[8];
+                unpack_biased8<BITS>(a.v_signed ? flip_signs<BITS>(cw) : cw, u);
+                const float2 sm = vmeta[warp][ti][vgrp];
                 const u64 cz = pk(sm.y, sm.y);
-                const u64 f01 = sub2(pk(__uint_as_float(u[0]), __uint_as_float(u[1])), cz);
-                const u64 f23 = sub2(pk(__uint_as_float(u[2]), __uint_as_float(u[3])), cz);
+                u64 f[4];                                     // code - zp, exact
+#pragma unroll
+                for (int k = 0; k < 4; ++k) f[k] = sub2(pk(__uint_as_float(u[2 * k]), __uint_as_float(u[2 * k + 1])), cz);
 #pragma unroll
                 for (int j = 0; j < G; ++j) {
                     const float w = __fmul_rn(pi[j], sm.x);
-                    acc_o[j][0] = fma2(f01, pk(w, w), acc_o[j][0]);
-                    acc_o[j][1] = fma2(f23, pk(w, w), acc_o[j][1]);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc_o[j][k] = fma2(f[k], pk(w, w), acc_o[j][k]);
                 }
-            } else {
-                const uint2 rv = __ldcs(reinterpret_cast<const uint2*>(a.vr + ((uint64_t)o * a.R + (t0 + i - Tq)) * kAC + c4));
-                const u64 r01 = widen_bf16x2(rv.x), r23 = widen_bf16x2(rv.y);
+            } else if (ti < nt) {
+                const uint4 rv = __ldcs(reinterpret_cast<const uint4*>(a.vr + ((uint64_t)o * a.R + (t0 + ti - Tq)) * kAC + c8));
+                const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
                 for (int j = 0; j < G; ++j) {
-                    acc_o[j][0] = fma2(r01, pk(pi[j], pi[j]), acc_o[j][0]);
-                    acc_o[j][1] = fma2(r23, pk(pi[j], pi[j]), acc_o[j][1]);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc_o[j][k] = fma2(widen_bf16x2(rw[k]), pk(pi[j], pi[j]), acc_o[j][k]);
                 }
             }
         }
@@ -316,8 +308,15 @@ attend_split_kernel(const AttnArgs a)
     for (int j = 0; j < G; ++j) {
         const float l = warp_sum(ell[j]);
         if (lane == 0) { wm[warp][j] = m[j]; wl[warp][j] = l; }
-        *reinterpret_cast<float4*>(&wo[warp][j][c4]) =
-            make_float4(lo_of(acc_o[j][0]), hi_of(acc_o[j][0]), lo_of(acc_o[j][1]), hi_of(acc_o[j][1]));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)                   // the two half-warps' tokens
+            acc_o[j][k] = add2(acc_o[j][k], __shfl_xor_sync(0xFFFFFFFFu, acc_o[j][k], 16));
+        if (half == 0) {
+            *reinterpret_cast<float4*>(&wo[warp][j][c8]) =
+                make_float4(lo_of(acc_o[j][0]), hi_of(acc_o[j][0]), lo_of(acc_o[j][1]), hi_of(acc_o[j][1]));
+            *reinterpret_cast<float4*>(&wo[warp][j][c8 + 4]) =
+                make_float4(lo_of(acc_o[j][2]), hi_of(acc_o[j][2]), lo_of(acc_o[j][3]), hi_of(acc_o[j][3]));
+        }
     }
     __syncthreads();
     for (int j = 0; j < G; ++j) {
