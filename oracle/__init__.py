@@ -74,9 +74,10 @@ def _load():
         lib.oracle_compact.argtypes = [vp, i64, i64, i64, i64, vp, i64, vp]
         lib.oracle_dequantize_f64.argtypes = [vp, vp, vp, vp, P, i32, vp]
         lib.oracle_attend.argtypes = [vp, i64, vp, vp, i64, i64, i64, vp]
+        lib.oracle_rotate.argtypes = [vp, i64, i64, vp, i32, vp]
         for f in ("oracle_sizes", "oracle_token_compression_ratio", "oracle_quantize",
                   "oracle_dequantize", "oracle_error_stats", "oracle_h2o_select",
-                  "oracle_snapkv_select", "oracle_compact", "oracle_dequantize_f64", "oracle_attend"):
+                  "oracle_snapkv_select", "oracle_compact", "oracle_dequantize_f64", "oracle_attend", "oracle_rotate"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -242,6 +243,19 @@ def attend(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
     assert k.shape == (outer, T, C) and v.shape == (outer, T, C)
     out = np.zeros((outer, group, C), np.float64)
     _check(_load().oracle_attend(_ptr(q), group, _ptr(k), _ptr(v), outer, T, C, _ptr(out)), "attend")
+    return out
+
+
+def rotate(x: np.ndarray, signs: np.ndarray, inverse: bool = False) -> np.ndarray:
+    """Randomized Hadamard rotation of the last axis (binary64): forward
+    (1/sqrt(C)) H (signs * x), inverse signs * ((1/sqrt(C)) H y)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    C = x.shape[-1]
+    signs = np.ascontiguousarray(signs, dtype=np.int8)
+    assert signs.shape == (C,)
+    out = np.zeros_like(x)
+    _check(_load().oracle_rotate(_ptr(x), x.size // C if C else 0, C, _ptr(signs), int(inverse), _ptr(out)),
+           "rotate")
     return out
 
 

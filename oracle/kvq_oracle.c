@@ -30,6 +30,9 @@
  *        §"K 的误差会改变权重，V 的误差会改变内容" (logit_t = q^T k_t / sqrt(d),
  *        y = sum_t a_t v_t with a = softmax of the logits), §"让 kernel 接住收益"
  *        (the attention kernel reads the quantized cache and dequantizes it).
+ *  KV-COBRA notes (papernotes.org), "关键设计" item 4: an orthogonal
+ *        Walsh-Hadamard rotation with fixed random sign flips equalises the
+ *        variances of the coordinates before scalar quantization.
  *
  * Readings taken where the pages are silent (each one also listed in the
  * design notes):
@@ -632,3 +635,45 @@ int oracle_attend(const double* q, int64_t group, const double* k, const double*
     free(logit);
     return OR_OK;
 }
+
+/* ------------------------------------------------------------------ */
+/* randomized Hadamard rotation (KV-COBRA notes, "关键设计" item 4)      */
+/* ------------------------------------------------------------------ */
+
+/* y = (1/sqrt(C)) H (signs .* x) per row (forward), or
+ * x = signs .* ((1/sqrt(C)) H y) (inverse), in binary64.  H is built by the
+ * Sylvester recursion H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]] and applied
+ * as a plain matrix-vector product.  A negative sign entry flips its channel.
+ * x, out: [rows][C]; C a power of two. */
+int oracle_rotate(const double* x, int64_t rows, int64_t C, const int8_t* signs, int inverse, double* out)
+{
+    if (rows < 0 || C < 1 || (C & (C - 1)) != 0) return OR_EINVAL;
+    signed char* H = (signed char*)malloc((size_t)(C * C));
+    double* u = (double*)malloc((size_t)C * sizeof(double));
+    if (!H || !u) { free(H); free(u); return OR_EINVAL; }
+    H[0] = 1;
+    for (int64_t n = 1; n < C; n *= 2)            /* H_n in the top-left n x n block -> H_2n */
+        for (int64_t i = 0; i < n; ++i)
+            for (int64_t j = 0; j < n; ++j) {
+                signed char h = H[i * C + j];
+                H[i * C + j + n] = h;
+                H[(i + n) * C + j] = h;
+                H[(i + n) * C + j + n] = (signed char)(-h);
+            }
+    const double scale = 1.0 / sqrt((double)C);
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* xr = x + r * C;
+        double* yr = out + r * C;
+        for (int64_t c = 0; c < C; ++c) u[c] = (!inverse && signs[c] < 0) ? -xr[c] : xr[c];
+        for (int64_t i = 0; i < C; ++i) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < C; ++c) acc += (double)H[i * C + c] * u[c];
+            acc *= scale;
+            yr[i] = (inverse && signs[i] < 0) ? -acc : acc;
+        }
+    }
+    free(H);
+    free(u);
+    return OR_OK;
+}
+

@@ -712,3 +712,66 @@ def test_dequantize_f64_agrees_with_the_float32_dequantizer():
         Tq = 300 - qp.residual
         assert np.all(np.abs(x64[:, :Tq] - x32[:, :Tq]) <= np.abs(x64[:, :Tq]) * 2.0 ** -24)
         assert np.array_equal(x64[:, Tq:], O.bf16_bits_to_f32(x[:, Tq:]).astype(np.float64))
+
+
+# ---------------------------------------------------------------- randomized Hadamard rotation
+# KV-COBRA notes, "关键设计" item 4: an orthogonal Walsh-Hadamard matrix with
+# fixed random sign flips equalises the coordinates' variances.
+
+
+def test_rotate_two_channels_closed_form():
+    """C = 2: the textbook 2-point transform [(a+b), (a-b)] / sqrt(2)."""
+    x = np.array([[3.0, -1.25], [0.5, 0.5]])
+    y = O.rotate(x, np.ones(2, np.int8))
+    assert np.allclose(y, np.stack([x[:, 0] + x[:, 1], x[:, 0] - x[:, 1]], axis=1) / math.sqrt(2), rtol=1e-15)
+
+
+def test_rotate_block_structure():
+    """Sylvester structure: for x = [a; b], rotate_C(x) = [R(a) + R(b); R(a) - R(b)] / sqrt(2)
+    with R the rotation of size C/2 (catches a sequency-ordered or transposed matrix)."""
+    rng = np.random.default_rng(50)
+    for C in (4, 16, 128):
+        x = rng.standard_normal((3, C))
+        ra = O.rotate(x[:, : C // 2], np.ones(C // 2, np.int8))
+        rb = O.rotate(x[:, C // 2:], np.ones(C // 2, np.int8))
+        want = np.concatenate([ra + rb, ra - rb], axis=1) / math.sqrt(2)
+        assert np.allclose(O.rotate(x, np.ones(C, np.int8)), want, rtol=1e-12, atol=1e-14)
+
+
+def test_rotate_is_orthogonal_and_inverted():
+    """Round trips both ways are the identity and the norm is kept (catches a
+    missing 1/sqrt(C), signs applied on the wrong side of the inverse)."""
+    rng = np.random.default_rng(51)
+    for C in (32, 128, 1024):
+        x = rng.standard_normal((5, C)) * rng.uniform(0.1, 10, (5, 1))
+        s = np.where(rng.random(C) < 0.5, -1, 1).astype(np.int8)
+        y = O.rotate(x, s)
+        assert np.allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+        assert np.allclose(O.rotate(y, s, inverse=True), x, rtol=1e-12, atol=1e-12)
+        assert np.allclose(O.rotate(O.rotate(x, s, inverse=True), s), x, rtol=1e-12, atol=1e-12)
+
+
+def test_rotate_constant_vector_and_signs():
+    """A constant row maps to sqrt(C) e_0; the signs act on the input:
+    forward(x, s) = forward(s * x, +1)."""
+    C = 64
+    y = O.rotate(np.ones((1, C)), np.ones(C, np.int8))
+    want = np.zeros((1, C))
+    want[0, 0] = math.sqrt(C)
+    assert np.allclose(y, want, atol=1e-13)
+    rng = np.random.default_rng(52)
+    x = rng.standard_normal((2, C))
+    s = np.where(rng.random(C) < 0.5, -1, 1).astype(np.int8)
+    assert np.allclose(O.rotate(x, s), O.rotate(x * s, np.ones(C, np.int8)), rtol=1e-14, atol=1e-15)
+
+
+def test_rotate_equalises_variances():
+    """The page's claim: for independent coordinates with variances lam_c the
+    rotated coordinates all have the mean variance, exactly:
+    sum_c rotate(sqrt(lam_c) e_c)_i^2 = mean(lam) for every i."""
+    C = 128
+    rng = np.random.default_rng(53)
+    lam = np.exp(rng.uniform(-7, 7, C))                  # spread of 1e6
+    s = np.where(rng.random(C) < 0.5, -1, 1).astype(np.int8)
+    cols = O.rotate(np.diag(np.sqrt(lam)), s)           # row c = rotation of sqrt(lam_c) e_c
+    assert np.allclose((cols ** 2).sum(axis=0), lam.mean(), rtol=1e-12)
