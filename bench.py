@@ -568,9 +568,15 @@ def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32,
         ws = torch.empty(b.kvq_attend_workspace(tuple(K.shape), G), dtype=torch.uint8, device=dev)
         ms = med(lambda: b.attend_decode(q, qk, qv, out=o, workspace=ws, stream=stream))
         out[f"2_kivi_int4/attend_decode_G{G}"] = entry(ms, cache_B + 2 * q.numel() * 4 + 2 * ws.numel())
-    del K, V, qk, qv
+    del qk, qv
     if only_attend:
         return out
+    # randomized Hadamard rotation of the key cache (bf16 -> bf16): read + write
+    signs = torch.where(torch.rand(K.shape[-1], device=dev, generator=torch.Generator(device=dev).manual_seed(3)) < 0.5,
+                        -1, 1).to(torch.int8)
+    rot = torch.empty_like(K)
+    out["2_kivi_int4/K/rotate"] = entry(med(lambda: b.rotate(K, signs, out=rot, stream=stream)), 2 * K.numel() * 2)
+    del K, V, rot
     # 3: full model INT8, per channel over all tokens
     K, V = W.fullmodel_kv(dev, seed=3)
     qdq("3_fullmodel_int8", [("K", K), ("V", V)], b.QParams.sym(8, axis=b.ALONG_T, group=0))

@@ -233,6 +233,26 @@ KVQ_API kvq_status kvq_attend_decode(const float* q, int64_t group, const void* 
                                      const void* v_resid, const kvq_qparams* v_params, const kvq_shape* shape,
                                      float* out, void* workspace, size_t workspace_B, void* stream);
 
+/* Data-free randomized Hadamard rotation of every row (the C channels of one
+ * token) of a [outer, T, C] tensor.  KV-COBRA notes (papernotes.org),
+ * "关键设计" item 4: an orthogonal Walsh-Hadamard matrix with fixed random
+ * sign flips mixes the coordinates, equalises their variances to the mean
+ * variance and makes each coordinate nearly Gaussian before scalar
+ * quantization; here without the calibrated projection (no data needed).
+ *     forward:  y = (1/sqrt(C)) * H_C * (signs .* x)
+ *     inverse:  x = signs .* ((1/sqrt(C)) * H_C * y)
+ * H_C is the Sylvester Hadamard matrix (H_1 = [1], H_2n = [[H, H], [H, -H]]),
+ * symmetric with H_C * H_C = C * I, so inverse(forward(x)) = x.
+ *  - x: [outer, T, C] in x_dtype (F32 or BF16); out: the same shape in
+ *    out_dtype (F32 or BF16), rounded once; out may equal x when the dtypes
+ *    match (each row is read completely before it is written).
+ *  - signs: device int8 [C]; a negative entry flips that channel, any other
+ *    value keeps it (+1 / -1 are the intended values).
+ *  - C must be a power of two from 32 to 1024 (KVQ_EUNSUPPORTED otherwise).
+ *  - Errors: KVQ_EINVAL (NULL or misaligned buffers, bad dtypes), KVQ_ECUDA. */
+KVQ_API kvq_status kvq_rotate(const void* x, kvq_dtype x_dtype, const kvq_shape* shape, const int8_t* signs,
+                              int inverse, void* out, kvq_dtype out_dtype, void* stream);
+
 /* Size of the library's fixed scratch array used by kvq_error_stats_noalloc. */
 #define KVQ_NOALLOC_SCRATCH_BYTES (1 << 20)
 

@@ -68,6 +68,7 @@ def _load() -> ctypes.CDLL:
         "kvq_error_stats_noalloc": [vp, i32, vp, vp, vp, vp, S, P, vp, vp],
         "kvq_attend_workspace": [S, i64, psz],
         "kvq_attend_decode": [vp, i64, vp, vp, vp, vp, P, vp, vp, vp, vp, P, S, vp, vp, sz, vp],
+        "kvq_rotate": [vp, i32, S, vp, i32, vp, i32, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -86,7 +87,7 @@ LIB = _load()
 EXPORTS = ("kvq_quantized_sizes", "kvq_quantize", "kvq_dequantize", "kvq_error_stats",
            "kvq_compression_ratio", "kvq_token_compression_ratio", "kv_select_workspace",
            "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kv_compact_kv", "kvq_last_error", "kvq_version",
-           "kvq_error_stats_noalloc", "kvq_attend_workspace", "kvq_attend_decode")
+           "kvq_error_stats_noalloc", "kvq_attend_workspace", "kvq_attend_decode", "kvq_rotate")
 
 # size of the library's fixed scratch array behind kvq_error_stats_noalloc
 NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -239,6 +240,12 @@ def kvq_attend_decode(q, group, k_codes, k_scale, k_zero, k_resid, kqp: QParams,
                                  _stream(stream)))
 
 
+def kvq_rotate(x, x_dtype, shape, signs, inverse, out, out_dtype, stream=None):
+    s = _shape(shape)
+    _check(LIB.kvq_rotate(_ptr(x), x_dtype, ctypes.byref(s), _ptr(signs), int(bool(inverse)), _ptr(out), out_dtype,
+                          _stream(stream)))
+
+
 def kvq_last_error() -> str:
     return LIB.kvq_last_error().decode(errors="replace")
 
@@ -375,3 +382,16 @@ def attend_decode(q, qk: Quantized, qv: Quantized, out=None, workspace=None, str
     kvq_attend_decode(q, group, qk.codes, qk.scale, qk.zero, qk.resid, qk.qp, qv.codes, qv.scale, qv.zero,
                       qv.resid, qv.qp, qk.shape, out, workspace, workspace.numel(), stream)
     return out
+
+
+def rotate(x, signs, inverse=False, out=None, out_dtype=None, stream=None):
+    """x: CUDA [..., T, C] bf16 or float32; signs: CUDA int8 [C] (+1 / -1) ->
+    the randomized Hadamard rotation of every row (or its inverse)."""
+    import torch
+    shape = (x.numel() // (x.shape[-1] * x.shape[-2]) if x.shape[-1] * x.shape[-2] else 0, x.shape[-2], x.shape[-1])
+    od = torch_dtype_code(x) if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16 if od == BF16 else torch.float32, device=x.device)
+    kvq_rotate(x, torch_dtype_code(x), shape, signs, inverse, out, od, stream)
+    return out
+

@@ -349,6 +349,27 @@ kvq_status kvq_attend_decode(const float* q, int64_t group, const void* k_codes,
     return cuda_status(kvq::launch_attend(a, (cudaStream_t)stream), "kvq_attend_decode launch");
 }
 
+kvq_status kvq_rotate(const void* x, kvq_dtype x_dtype, const kvq_shape* shape, const int8_t* signs, int inverse,
+                      void* out, kvq_dtype out_dtype, void* stream)
+{
+    if (!shape) return fail(KVQ_EINVAL, "shape must not be NULL");
+    if (shape->outer < 0 || shape->T < 0 || shape->C < 0) return fail(KVQ_EINVAL, "negative extent");
+    if (!mul_ok(shape->outer, shape->T, shape->C)) return fail(KVQ_EINVAL, "tensor too large");
+    if (x_dtype != KVQ_F32 && x_dtype != KVQ_BF16) return fail(KVQ_EINVAL, "x dtype must be F32 or BF16");
+    if (out_dtype != KVQ_F32 && out_dtype != KVQ_BF16) return fail(KVQ_EINVAL, "out dtype must be F32 or BF16");
+    const int64_t rows = shape->outer * shape->T, C = shape->C;
+    if (rows == 0 || C == 0) return KVQ_OK;
+    if (C < 32 || C > 1024 || (C & (C - 1)) != 0)
+        return fail(KVQ_EUNSUPPORTED, "the rotation needs C a power of two from 32 to 1024 (got %lld)", (long long)C);
+    kvq_status s;
+    if ((s = need_ptr(x, 1, "x")) || (s = need_ptr(out, 1, "out")) || (s = need_ptr(signs, 1, "signs")))
+        return s;
+    if (!aligned16(x) || !aligned16(out)) return fail(KVQ_EINVAL, "x and out must be 16-byte aligned");
+    return cuda_status(kvq::launch_rotate(x, x_dtype, out, out_dtype, signs, (uint64_t)rows, C, inverse ? 1 : 0,
+                                          (cudaStream_t)stream),
+                       "kvq_rotate launch");
+}
+
 double kvq_compression_ratio(size_t orig_B, size_t codes_B, size_t scale_B, size_t zero_B, size_t resid_B)
 {
     const double d = (double)codes_B + (double)scale_B + (double)zero_B + (double)resid_B;

@@ -91,6 +91,10 @@ int64_t attend_splits(int64_t T);
 size_t attend_workspace(int64_t outer, int64_t T, int64_t group);
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st);
 
+// ---- randomized Hadamard rotation of [rows, C] (rotate.cu); C a power of two in [32, 1024]
+cudaError_t launch_rotate(const void* x, int x_dt, void* out, int out_dt, const int8_t* signs, uint64_t rows,
+                          int64_t C, int inverse, cudaStream_t st);
+
 // ---- keep-set selection (select.cu) and compaction (compact.cu)
 struct SelectArgs {
     const float* hist;

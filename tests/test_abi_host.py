@@ -33,7 +33,7 @@ def declared_symbols():
 
 def test_library_exports_every_declared_symbol(kb):
     declared = declared_symbols()
-    assert len(declared) == 16
+    assert len(declared) == 17
     for name in declared:
         assert hasattr(kb.LIB, name), name
     assert declared == set(kb.EXPORTS)
@@ -235,4 +235,21 @@ def test_attend_rejected_before_launch(kb):
         with pytest.raises(kb.KvqError) as e:
             call(**kw)
         assert e.value.status == status, (kw, str(e.value))
+
+
+def test_rotate_rejected_before_launch(kb):
+    fake = 1 << 20  # never dereferenced: validation fails first
+    for shape, xd, od, signs, x, status in (
+            ((2, 10, 48), kb.BF16, kb.BF16, fake, fake, kb.EUNSUPPORTED),     # C not a power of two
+            ((2, 10, 16), kb.BF16, kb.BF16, fake, fake, kb.EUNSUPPORTED),     # C below 32
+            ((2, 10, 2048), kb.F32, kb.F32, fake, fake, kb.EUNSUPPORTED),     # C above 1024
+            ((2, 10, 128), kb.I8, kb.BF16, fake, fake, kb.EINVAL),            # source dtype
+            ((2, 10, 128), kb.BF16, kb.I8, fake, fake, kb.EINVAL),            # output dtype
+            ((2, 10, 128), kb.BF16, kb.BF16, None, fake, kb.EINVAL),          # no signs
+            ((2, 10, 128), kb.BF16, kb.BF16, fake, None, kb.EINVAL),          # no input
+            ((2, 10, 128), kb.BF16, kb.BF16, fake, fake + 4, kb.EINVAL)):     # misaligned
+        with pytest.raises(kb.KvqError) as e:
+            kb.kvq_rotate(x, xd, shape, signs, False, fake, od, 0)
+        assert e.value.status == status, (shape, str(e.value))
+    kb.kvq_rotate(None, kb.BF16, (0, 10, 128), None, False, None, kb.BF16, 0)   # empty: nothing to do
 

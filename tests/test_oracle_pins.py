@@ -708,7 +708,8 @@ def test_dequantize_f64_agrees_with_the_float32_dequantizer():
                O.QParams.sym(2, axis=O.ALONG_C, group=32, residual=3, scale_dtype=O.BF16)):
         qt = O.quantize(x, O.BF16, qp)
         x64 = O.dequantize_f64(qt, x.shape, qp, O.BF16)
-        x32 = O.dequantize(qt, x.shape, qp, O.F32).astype(np.float64)   # its residual rows need f32 input
+        with np.errstate(invalid="ignore"):      # its residual rows would need f32 input: not compared
+            x32 = O.dequantize(qt, x.shape, qp, O.F32).astype(np.float64)
         Tq = 300 - qp.residual
         assert np.all(np.abs(x64[:, :Tq] - x32[:, :Tq]) <= np.abs(x64[:, :Tq]) * 2.0 ** -24)
         assert np.array_equal(x64[:, Tq:], O.bf16_bits_to_f32(x[:, Tq:]).astype(np.float64))
