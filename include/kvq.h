@@ -253,6 +253,40 @@ KVQ_API kvq_status kvq_attend_decode(const float* q, int64_t group, const void* 
 KVQ_API kvq_status kvq_rotate(const void* x, kvq_dtype x_dtype, const kvq_shape* shape, const int8_t* signs,
                               int inverse, void* out, kvq_dtype out_dtype, void* stream);
 
+/* Online (streaming) quantized cache: append tokens, quantize full blocks.
+ * [KVC] §"带残差区的压缩预算，逐项加起来": the most recent tokens stay in bf16 and
+ * the older ones are stored quantized in groups; with one token per decode step
+ * a key group of g tokens (per channel) can only be quantized once all g have
+ * arrived, so arriving tokens are buffered together with the residual window.
+ * State, all caller-owned:
+ *  - the store: codes / scale / zero laid out exactly as kvq_quantize lays out
+ *    a [outer, T_cap, C] tensor quantized with p and no residual
+ *    (shape = {outer, T_cap, C}); its first *tq tokens are filled;
+ *  - resid: [outer][p->residual + block][C] in x_dtype; its first *nres rows
+ *    are the newest tokens, oldest first;
+ *  - *tq (a multiple of block) and *nres (< p->residual + block): host counters,
+ *    updated by the call.
+ * The call copies the n new rows x_new [outer][n][C] into the buffer; each time
+ * the buffer reaches p->residual + block rows, its oldest `block` rows are
+ * quantized (groups of p->group along T for keys, along C for values) into
+ * store tokens [*tq, *tq + block) and leave the buffer.  Appending the T tokens
+ * of a sequence in any chunks therefore leaves exactly what kvq_quantize gives
+ * for the whole sequence with residual T - *tq, bit for bit.
+ *  - block: tokens per flush; groups along T need block to be a multiple of
+ *    p->group (> 0).
+ *  - workspace: at least kvq_append_workspace bytes.
+ *  - Errors: KVQ_EINVAL (bad counters, a store too small for the flushes the
+ *    call needs, NULL or misaligned buffers), KVQ_EWORKSPACE; nothing is
+ *    launched and the counters are unchanged then.
+ *  - Cost: one quantize and four small copies per flush; a long prompt is
+ *    better quantized with kvq_quantize before appending starts. */
+KVQ_API kvq_status kvq_append_workspace(const kvq_shape* shape, kvq_dtype x_dtype, const kvq_qparams* p,
+                                        int64_t block, size_t* workspace_B);
+KVQ_API kvq_status kvq_append(const void* x_new, int64_t n, kvq_dtype x_dtype, const kvq_shape* shape,
+                              const kvq_qparams* p, int64_t block, void* codes, void* scale, void* zero,
+                              void* resid, int64_t* tq, int64_t* nres, void* workspace, size_t workspace_B,
+                              void* stream);
+
 /* Size of the library's fixed scratch array used by kvq_error_stats_noalloc. */
 #define KVQ_NOALLOC_SCRATCH_BYTES (1 << 20)
 

@@ -69,6 +69,9 @@ def _load() -> ctypes.CDLL:
         "kvq_attend_workspace": [S, i64, psz],
         "kvq_attend_decode": [vp, i64, vp, vp, vp, vp, P, vp, vp, vp, vp, P, S, vp, vp, sz, vp],
         "kvq_rotate": [vp, i32, S, vp, i32, vp, i32, vp],
+        "kvq_append_workspace": [S, i32, P, i64, psz],
+        "kvq_append": [vp, i64, i32, S, P, i64, vp, vp, vp, vp, ctypes.POINTER(i64), ctypes.POINTER(i64), vp, sz,
+                       vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -87,7 +90,8 @@ LIB = _load()
 EXPORTS = ("kvq_quantized_sizes", "kvq_quantize", "kvq_dequantize", "kvq_error_stats",
            "kvq_compression_ratio", "kvq_token_compression_ratio", "kv_select_workspace",
            "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kv_compact_kv", "kvq_last_error", "kvq_version",
-           "kvq_error_stats_noalloc", "kvq_attend_workspace", "kvq_attend_decode", "kvq_rotate")
+           "kvq_error_stats_noalloc", "kvq_attend_workspace", "kvq_attend_decode", "kvq_rotate",
+           "kvq_append_workspace", "kvq_append")
 
 # size of the library's fixed scratch array behind kvq_error_stats_noalloc
 NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -244,6 +248,23 @@ def kvq_rotate(x, x_dtype, shape, signs, inverse, out, out_dtype, stream=None):
     s = _shape(shape)
     _check(LIB.kvq_rotate(_ptr(x), x_dtype, ctypes.byref(s), _ptr(signs), int(bool(inverse)), _ptr(out), out_dtype,
                           _stream(stream)))
+
+
+def kvq_append_workspace(shape, x_dtype, qp: QParams, block: int) -> int:
+    s, p, n = _shape(shape), qp.c(), ctypes.c_size_t()
+    _check(LIB.kvq_append_workspace(ctypes.byref(s), x_dtype, ctypes.byref(p), int(block), ctypes.byref(n)))
+    return n.value
+
+
+def kvq_append(x_new, n, x_dtype, shape, qp: QParams, block, codes, scale, zero, resid, tq, nres, workspace,
+               workspace_B, stream=None):
+    """Returns the updated (tq, nres) counters."""
+    s, p = _shape(shape), qp.c()
+    t, r = ctypes.c_int64(int(tq)), ctypes.c_int64(int(nres))
+    _check(LIB.kvq_append(_ptr(x_new), int(n), x_dtype, ctypes.byref(s), ctypes.byref(p), int(block), _ptr(codes),
+                          _ptr(scale), _ptr(zero), _ptr(resid), ctypes.byref(t), ctypes.byref(r), _ptr(workspace),
+                          int(workspace_B), _stream(stream)))
+    return t.value, r.value
 
 
 def kvq_last_error() -> str:

@@ -370,6 +370,147 @@ kvq_status kvq_rotate(const void* x, kvq_dtype x_dtype, const kvq_shape* shape, 
                        "kvq_rotate launch");
 }
 
+namespace {
+
+// The store's format and the one flush of the streaming cache: the buffer
+// [outer, R + block, C] quantized with residual R, into workspace buffers.
+struct AppendPlan {
+    kvq::QSpec store, flush;
+    Sizes fz;
+    size_t off_codes, off_scale, off_zero, off_resid, off_qws, qws, total;
+};
+
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+kvq_status append_plan(const kvq_shape* shape, kvq_dtype x_dtype, const kvq_qparams* p, int64_t block,
+                       AppendPlan& P)
+{
+    if (!shape || !p) return fail(KVQ_EINVAL, "shape and qparams must not be NULL");
+    if (p->residual < 0) return fail(KVQ_EINVAL, "residual must be >= 0");
+    if (block < 1) return fail(KVQ_EINVAL, "block must be >= 1 (got %lld)", (long long)block);
+    kvq_qparams sp = *p;
+    sp.residual = 0;
+    kvq_status s = make_spec(shape, x_dtype, &sp, P.store);
+    if (s != KVQ_OK) return s;
+    if (p->axis == KVQ_GROUP_ALONG_T && (p->group <= 0 || block % p->group != 0))
+        return fail(KVQ_EINVAL, "groups along T need block (%lld) to be a multiple of the group (%lld > 0)",
+                    (long long)block, (long long)p->group);
+    const kvq_shape fs = {shape->outer, p->residual + block, shape->C};
+    if ((s = make_spec(&fs, x_dtype, p, P.flush)) != KVQ_OK) return s;
+    P.fz = sizes_of(P.flush);
+    P.qws = kvq::quantize_workspace(P.flush);
+    P.off_codes = 0;
+    P.off_scale = round256(P.fz.codes);
+    P.off_zero = P.off_scale + round256(P.fz.scale);
+    P.off_resid = P.off_zero + round256(P.fz.zero);
+    P.off_qws = P.off_resid + round256(P.fz.resid);
+    P.total = P.off_qws + round256(P.qws);
+    return KVQ_OK;
+}
+
+}  // namespace
+
+kvq_status kvq_append_workspace(const kvq_shape* shape, kvq_dtype x_dtype, const kvq_qparams* p, int64_t block,
+                                size_t* workspace_B)
+{
+    AppendPlan P;
+    kvq_status s = append_plan(shape, x_dtype, p, block, P);
+    if (s != KVQ_OK) return s;
+    if (!workspace_B) return fail(KVQ_EINVAL, "workspace_B must not be NULL");
+    *workspace_B = P.total;
+    return KVQ_OK;
+}
+
+kvq_status kvq_append(const void* x_new, int64_t n, kvq_dtype x_dtype, const kvq_shape* shape, const kvq_qparams* p,
+                      int64_t block, void* codes, void* scale, void* zero, void* resid, int64_t* tq, int64_t* nres,
+                      void* workspace, size_t workspace_B, void* stream)
+{
+    AppendPlan P;
+    kvq_status s = append_plan(shape, x_dtype, p, block, P);
+    if (s != KVQ_OK) return s;
+    if (!tq || !nres) return fail(KVQ_EINVAL, "tq and nres must not be NULL");
+    const int64_t R = p->residual, cap = R + block, Tcap = shape->T;
+    if (n < 0) return fail(KVQ_EINVAL, "n must be >= 0");
+    if (*tq < 0 || *tq % block != 0 || *tq > Tcap)
+        return fail(KVQ_EINVAL, "tq (%lld) must be a multiple of block in [0, T_cap]", (long long)*tq);
+    if (*nres < 0 || *nres >= cap)
+        return fail(KVQ_EINVAL, "nres (%lld) must be in [0, residual + block)", (long long)*nres);
+    // the flushes this call performs, and the store room they need
+    int64_t flushes = 0;
+    for (int64_t cur = *nres, rem = n; rem > 0;) {
+        const int64_t m = std::min(rem, cap - cur);
+        cur += m;
+        rem -= m;
+        if (cur == cap) { ++flushes; cur = R; }
+    }
+    if (*tq + flushes * block > Tcap)
+        return fail(KVQ_EINVAL, "the store holds %lld tokens: %lld more would be quantized after %lld",
+                    (long long)Tcap, (long long)(flushes * block), (long long)*tq);
+    const size_t es = dtype_bytes(x_dtype);
+    const int64_t outer = shape->outer, C = shape->C;
+    const Sizes sz = sizes_of(P.store);
+    if ((s = need_ptr(x_new, (size_t)(outer * n * C) * es, "x_new")) || (s = need_ptr(resid, (size_t)(outer * cap * C) * es, "resid")) ||
+        (flushes && ((s = need_ptr(codes, sz.codes, "codes")) || (s = need_ptr(scale, sz.scale, "scale")) ||
+                     (s = need_ptr(zero, sz.zero, "zero")))))
+        return s;
+    if ((s = need_align(x_new, es, "x_new")) || (s = need_align(resid, es, "resid")) ||
+        (s = need_align(scale, dtype_bytes(P.store.scale_dt), "scale")) ||
+        (s = need_align(zero, dtype_bytes(P.store.zero_dt), "zero")) || (s = need_align(workspace, 256, "workspace")))
+        return s;
+    if (flushes && (!workspace || workspace_B < P.total))
+        return fail(KVQ_EWORKSPACE, "kvq_append needs %zu workspace bytes (got %zu)", P.total, workspace_B);
+
+    cudaStream_t st = (cudaStream_t)stream;
+    char* ws = static_cast<char*>(workspace);
+    char* rbuf = static_cast<char*>(resid);
+    const char* src = static_cast<const char*>(x_new);
+    const uint64_t rowx = (uint64_t)C * es;                      // bytes of one token row
+    const uint64_t rowc = (uint64_t)C * P.store.bits / 8;        // bytes of one token's codes
+    int64_t t = *tq, cur = *nres;
+    kvq::QSpec fq = P.flush;
+    fq.aligned = aligned16(resid) ? 1 : 0;
+    for (int64_t j = 0; j < n;) {
+        const int64_t m = std::min(n - j, cap - cur);
+        cudaError_t e = kvq::launch_copy2d(rbuf + cur * rowx, cap * rowx, src + j * rowx, n * rowx, m * rowx,
+                                           outer, st);
+        if (e != cudaSuccess) return cuda_status(e, "kvq_append copy");
+        cur += m;
+        j += m;
+        if (cur < cap) continue;
+        // flush: the oldest `block` rows -> store tokens [t, t + block), the newest R rows -> front of the buffer
+        kvq::QArgs a = {resid, ws + P.off_codes, ws + P.off_scale, ws + P.off_zero, ws + P.off_resid, nullptr,
+                        ws + P.off_qws, P.qws, fq};
+        if ((e = kvq::launch_quantize(a, st)) != cudaSuccess) return cuda_status(e, "kvq_append quantize");
+        e = kvq::launch_copy2d(static_cast<char*>(codes) + t * rowc, Tcap * rowc, ws + P.off_codes, block * rowc,
+                               block * rowc, outer, st);
+        const size_t sb = dtype_bytes(P.store.scale_dt), zb = dtype_bytes(P.store.zero_dt);
+        uint64_t mrow, mpitch, moff;                              // metadata elements per slice and flush
+        if (P.store.axis == KVQ_GROUP_ALONG_T) {
+            mrow = (uint64_t)(block / P.store.g) * C;
+            mpitch = (uint64_t)P.store.ngroups * C;
+            moff = (uint64_t)(t / P.store.g) * C;
+        } else {
+            mrow = (uint64_t)block * P.store.ngroups;
+            mpitch = (uint64_t)Tcap * P.store.ngroups;
+            moff = (uint64_t)t * P.store.ngroups;
+        }
+        if (e == cudaSuccess)
+            e = kvq::launch_copy2d(static_cast<char*>(scale) + moff * sb, mpitch * sb, ws + P.off_scale, mrow * sb,
+                                   mrow * sb, outer, st);
+        if (e == cudaSuccess && P.store.mode == KVQ_ASYM)
+            e = kvq::launch_copy2d(static_cast<char*>(zero) + moff * zb, mpitch * zb, ws + P.off_zero, mrow * zb,
+                                   mrow * zb, outer, st);
+        if (e == cudaSuccess)
+            e = kvq::launch_copy2d(rbuf, cap * rowx, ws + P.off_resid, R * rowx, R * rowx, outer, st);
+        if (e != cudaSuccess) return cuda_status(e, "kvq_append flush");
+        t += block;
+        cur = R;
+    }
+    *tq = t;
+    *nres = cur;
+    return KVQ_OK;
+}
+
 double kvq_compression_ratio(size_t orig_B, size_t codes_B, size_t scale_B, size_t zero_B, size_t resid_B)
 {
     const double d = (double)codes_B + (double)scale_B + (double)zero_B + (double)resid_B;

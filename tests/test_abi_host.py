@@ -33,7 +33,7 @@ def declared_symbols():
 
 def test_library_exports_every_declared_symbol(kb):
     declared = declared_symbols()
-    assert len(declared) == 17
+    assert len(declared) == 19
     for name in declared:
         assert hasattr(kb.LIB, name), name
     assert declared == set(kb.EXPORTS)
@@ -252,4 +252,31 @@ def test_rotate_rejected_before_launch(kb):
             kb.kvq_rotate(x, xd, shape, signs, False, fake, od, 0)
         assert e.value.status == status, (shape, str(e.value))
     kb.kvq_rotate(None, kb.BF16, (0, 10, 128), None, False, None, kb.BF16, 0)   # empty: nothing to do
+
+
+def test_append_rejected_before_launch(kb):
+    """Streaming append: bad counters, block/group mismatch, a store too small
+    for the flushes, missing workspace -- rejected with the counters unchanged."""
+    fake = 1 << 20  # never dereferenced: validation fails first
+    qp = kb.QParams.asym(4, 0, 15, axis=kb.ALONG_T, group=32, residual=16, scale_dtype=kb.BF16, zero_dtype=kb.BF16)
+    shape = (2, 64, 128)                                   # store of 64 tokens
+    wB = kb.kvq_append_workspace(shape, kb.BF16, qp, 32)
+    assert wB > 0
+    with pytest.raises(kb.KvqError) as e:
+        kb.kvq_append_workspace(shape, kb.BF16, qp, 48)   # block not a multiple of the group
+    assert e.value.status == kb.EINVAL
+    args = dict(codes=fake, scale=fake, zero=fake, resid=fake, ws=fake, wsB=wB)
+
+    def call(n=1, tq=0, nres=0, **kw):
+        a = dict(args, **kw)
+        return kb.kvq_append(fake, n, kb.BF16, shape, qp, 32, a["codes"], a["scale"], a["zero"], a["resid"], tq,
+                             nres, a["ws"], a["wsB"], 0)
+
+    for kw, status in ((dict(tq=5), kb.EINVAL), (dict(nres=48), kb.EINVAL), (dict(n=-1), kb.EINVAL),
+                       (dict(n=120), kb.EINVAL),             # 3 flushes of 32 need 96 > 64 store tokens
+                       (dict(n=50, resid=None), kb.EINVAL),  # 50 tokens fill the 48-row buffer once
+                       (dict(n=50, ws=None), kb.EWORKSPACE), (dict(n=50, wsB=wB - 1), kb.EWORKSPACE)):
+        with pytest.raises(kb.KvqError) as e:
+            call(**kw)
+        assert e.value.status == status, (kw, str(e.value))
 
