@@ -287,6 +287,35 @@ KVQ_API kvq_status kvq_append(const void* x_new, int64_t n, kvq_dtype x_dtype, c
                               void* resid, int64_t* tq, int64_t* nres, void* workspace, size_t workspace_B,
                               void* stream);
 
+/* Per-token mixed precision.  "大模型KV缓存自适应量化实战" §2.1: every token
+ * is stored at one of four levels, 2/4/8/16 bits; §3.1: per-token
+ * quantization, symmetric for 2 and 4 bits (qmax 1 and 7), asymmetric for 8
+ * bits ([0, 255]), 16 bits stored as is; §3.2: 2-bit precision tags
+ * (00/01/10/11 = 2/4/8/16 bits) and same-precision data kept together.  The
+ * controller that picks the levels is not part of this library: the caller
+ * passes tags[outer][T] (uint8, low 2 bits used).
+ * Layout of slice o of a bf16 [outer, T, C] tensor:
+ *  - stream: slice o's records start at byte o * T * 2C; token t's record is
+ *    at byte off[o][t] of it: the packed codes (as in the uniform formats:
+ *    channel c at bit (c mod 8/bits)*bits of byte c*bits/8, two's complement
+ *    for the symmetric levels), then the bf16 scale (and for 8 bits the bf16
+ *    zero point), or the C bf16 values for 16 bits.  Record bytes: C/4 + 2,
+ *    C/2 + 2, C + 4, 2C;
+ *  - off[o][0..T] (int64): exclusive prefix sums of the record sizes;
+ *    off[o][T] is the number of bytes slice o uses;
+ *  - tags2[o][ceil(T/4)]: the 2-bit tags, token t at bit 2*(t%4) of byte t/4.
+ * Scales and zero points are rounded to bf16 before the codes are computed,
+ * exactly as the uniform quantizer does.
+ *  - x, out: bf16; C must be 64, 128 or 256 (KVQ_EUNSUPPORTED otherwise).
+ *  - Sizes: kvq_mixed_sizes (stream bytes are those of the all-16-bit case;
+ *    off[o][T] tells how many a slice really uses).
+ *  - Errors: KVQ_EINVAL (NULL or misaligned buffers), KVQ_ECUDA. */
+KVQ_API kvq_status kvq_mixed_sizes(const kvq_shape* shape, size_t* stream_B, size_t* off_B, size_t* tags2_B);
+KVQ_API kvq_status kvq_mixed_quantize(const void* x, const uint8_t* tags, const kvq_shape* shape, void* stream_buf,
+                                      int64_t* off, uint8_t* tags2, void* stream);
+KVQ_API kvq_status kvq_mixed_dequantize(const void* stream_buf, const int64_t* off, const uint8_t* tags2,
+                                        const kvq_shape* shape, void* out, void* stream);
+
 /* Size of the library's fixed scratch array used by kvq_error_stats_noalloc. */
 #define KVQ_NOALLOC_SCRATCH_BYTES (1 << 20)
 

@@ -70,6 +70,9 @@ def _load() -> ctypes.CDLL:
         "kvq_attend_decode": [vp, i64, vp, vp, vp, vp, P, vp, vp, vp, vp, P, S, vp, vp, sz, vp],
         "kvq_rotate": [vp, i32, S, vp, i32, vp, i32, vp],
         "kvq_append_workspace": [S, i32, P, i64, psz],
+        "kvq_mixed_sizes": [S, psz, psz, psz],
+        "kvq_mixed_quantize": [vp, vp, S, vp, vp, vp, vp],
+        "kvq_mixed_dequantize": [vp, vp, vp, S, vp, vp],
         "kvq_append": [vp, i64, i32, S, P, i64, vp, vp, vp, vp, ctypes.POINTER(i64), ctypes.POINTER(i64), vp, sz,
                        vp],
     }
@@ -91,7 +94,7 @@ EXPORTS = ("kvq_quantized_sizes", "kvq_quantize", "kvq_dequantize", "kvq_error_s
            "kvq_compression_ratio", "kvq_token_compression_ratio", "kv_select_workspace",
            "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kv_compact_kv", "kvq_last_error", "kvq_version",
            "kvq_error_stats_noalloc", "kvq_attend_workspace", "kvq_attend_decode", "kvq_rotate",
-           "kvq_append_workspace", "kvq_append")
+           "kvq_append_workspace", "kvq_append", "kvq_mixed_sizes", "kvq_mixed_quantize", "kvq_mixed_dequantize")
 
 # size of the library's fixed scratch array behind kvq_error_stats_noalloc
 NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -265,6 +268,25 @@ def kvq_append(x_new, n, x_dtype, shape, qp: QParams, block, codes, scale, zero,
                           _ptr(scale), _ptr(zero), _ptr(resid), ctypes.byref(t), ctypes.byref(r), _ptr(workspace),
                           int(workspace_B), _stream(stream)))
     return t.value, r.value
+
+
+def kvq_mixed_sizes(shape):
+    s = _shape(shape)
+    a, b_, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(LIB.kvq_mixed_sizes(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b_), ctypes.byref(c)))
+    return a.value, b_.value, c.value
+
+
+def kvq_mixed_quantize(x, tags, shape, stream_buf, off, tags2, stream=None):
+    s = _shape(shape)
+    _check(LIB.kvq_mixed_quantize(_ptr(x), _ptr(tags), ctypes.byref(s), _ptr(stream_buf), _ptr(off), _ptr(tags2),
+                                  _stream(stream)))
+
+
+def kvq_mixed_dequantize(stream_buf, off, tags2, shape, out, stream=None):
+    s = _shape(shape)
+    _check(LIB.kvq_mixed_dequantize(_ptr(stream_buf), _ptr(off), _ptr(tags2), ctypes.byref(s), _ptr(out),
+                                    _stream(stream)))
 
 
 def kvq_last_error() -> str:

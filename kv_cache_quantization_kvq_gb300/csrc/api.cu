@@ -511,6 +511,83 @@ kvq_status kvq_append(const void* x_new, int64_t n, kvq_dtype x_dtype, const kvq
     return KVQ_OK;
 }
 
+namespace {
+
+kvq_status mixed_shape(const kvq_shape* shape)
+{
+    if (!shape) return fail(KVQ_EINVAL, "shape must not be NULL");
+    if (shape->outer < 0 || shape->T < 0 || shape->C < 0) return fail(KVQ_EINVAL, "negative extent");
+    if (!mul_ok(shape->outer, shape->T + 1, std::max<int64_t>(shape->C, 8) * 2)) return fail(KVQ_EINVAL, "tensor too large");
+    if (shape->C != 64 && shape->C != 128 && shape->C != 256)
+        return fail(KVQ_EUNSUPPORTED, "mixed precision supports C = 64, 128 or 256 (got %lld)", (long long)shape->C);
+    return KVQ_OK;
+}
+
+// the per-token format of a tag: 2 and 4 bits symmetric, 8 bits asymmetric [0, 255], bf16 metadata
+kvq::QSpec mixed_format(int bits, int64_t C)
+{
+    kvq_qparams p = {};
+    p.bits = bits;
+    p.mode = bits == 8 ? KVQ_ASYM : KVQ_SYM;
+    p.qmin = bits == 8 ? 0 : -((1 << (bits - 1)) - 1);
+    p.qmax = bits == 8 ? 255 : (1 << (bits - 1)) - 1;
+    p.axis = KVQ_GROUP_ALONG_C;
+    p.group = C;
+    p.residual = 0;
+    p.scale_dtype = KVQ_BF16;
+    p.zero_dtype = bits == 8 ? KVQ_BF16 : KVQ_NONE;
+    const kvq_shape sh = {1, 1, C};
+    kvq::QSpec q;
+    make_spec(&sh, KVQ_BF16, &p, q);                               // valid by construction
+    return q;
+}
+
+}  // namespace
+
+kvq_status kvq_mixed_sizes(const kvq_shape* shape, size_t* stream_B, size_t* off_B, size_t* tags2_B)
+{
+    kvq_status s = mixed_shape(shape);
+    if (s != KVQ_OK) return s;
+    if (stream_B) *stream_B = (size_t)(shape->outer * shape->T * shape->C * 2);
+    if (off_B) *off_B = (size_t)(shape->outer * (shape->T + 1)) * 8;
+    if (tags2_B) *tags2_B = (size_t)(shape->outer * ((shape->T + 3) / 4));
+    return KVQ_OK;
+}
+
+kvq_status kvq_mixed_quantize(const void* x, const uint8_t* tags, const kvq_shape* shape, void* stream_buf,
+                              int64_t* off, uint8_t* tags2, void* stream)
+{
+    kvq_status s = mixed_shape(shape);
+    if (s != KVQ_OK) return s;
+    const int64_t n = shape->outer * shape->T;
+    if (n == 0) return KVQ_OK;
+    if ((s = need_ptr(x, 1, "x")) || (s = need_ptr(tags, 1, "tags")) || (s = need_ptr(stream_buf, 1, "stream_buf")) ||
+        (s = need_ptr(off, 1, "off")) || (s = need_ptr(tags2, 1, "tags2")))
+        return s;
+    if ((s = need_align(x, 2, "x")) || (s = need_align(stream_buf, 2, "stream_buf")) || (s = need_align(off, 8, "off")))
+        return s;
+    const kvq::QSpec f2 = mixed_format(2, shape->C), f4 = mixed_format(4, shape->C), f8 = mixed_format(8, shape->C);
+    return cuda_status(kvq::launch_mixed_quantize(x, tags, shape->outer, shape->T, shape->C, stream_buf, off, tags2,
+                                                  f2, f4, f8, (cudaStream_t)stream),
+                       "kvq_mixed_quantize launch");
+}
+
+kvq_status kvq_mixed_dequantize(const void* stream_buf, const int64_t* off, const uint8_t* tags2,
+                                const kvq_shape* shape, void* out, void* stream)
+{
+    kvq_status s = mixed_shape(shape);
+    if (s != KVQ_OK) return s;
+    if (shape->outer * shape->T == 0) return KVQ_OK;
+    if ((s = need_ptr(stream_buf, 1, "stream_buf")) || (s = need_ptr(off, 1, "off")) ||
+        (s = need_ptr(tags2, 1, "tags2")) || (s = need_ptr(out, 1, "out")))
+        return s;
+    if ((s = need_align(stream_buf, 2, "stream_buf")) || (s = need_align(off, 8, "off")) || (s = need_align(out, 2, "out")))
+        return s;
+    return cuda_status(kvq::launch_mixed_dequantize(stream_buf, off, tags2, shape->outer, shape->T, shape->C, out,
+                                                    (cudaStream_t)stream),
+                       "kvq_mixed_dequantize launch");
+}
+
 double kvq_compression_ratio(size_t orig_B, size_t codes_B, size_t scale_B, size_t zero_B, size_t resid_B)
 {
     const double d = (double)codes_B + (double)scale_B + (double)zero_B + (double)resid_B;

@@ -99,6 +99,14 @@ cudaError_t launch_rotate(const void* x, int x_dt, void* out, int out_dt, const 
 cudaError_t launch_copy2d(void* dst, uint64_t dpitch, const void* src, uint64_t spitch, uint64_t width,
                           uint64_t rows, cudaStream_t st);
 
+// ---- per-token mixed precision (mixed.cu); tags 0..3 = 2/4/8/16 bits, C in {64, 128, 256}
+int64_t mixed_record_bytes(int tag, int64_t C);
+cudaError_t launch_mixed_quantize(const void* x, const uint8_t* tags, int64_t outer, int64_t T, int64_t C,
+                                  void* stream_buf, int64_t* off, uint8_t* tags2, const QSpec& f2, const QSpec& f4,
+                                  const QSpec& f8, cudaStream_t st);
+cudaError_t launch_mixed_dequantize(const void* stream_buf, const int64_t* off, const uint8_t* tags2, int64_t outer,
+                                    int64_t T, int64_t C, void* out, cudaStream_t st);
+
 // ---- keep-set selection (select.cu) and compaction (compact.cu)
 struct SelectArgs {
     const float* hist;

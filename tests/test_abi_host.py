@@ -33,7 +33,7 @@ def declared_symbols():
 
 def test_library_exports_every_declared_symbol(kb):
     declared = declared_symbols()
-    assert len(declared) == 19
+    assert len(declared) == 22
     for name in declared:
         assert hasattr(kb.LIB, name), name
     assert declared == set(kb.EXPORTS)
@@ -279,4 +279,17 @@ def test_append_rejected_before_launch(kb):
         with pytest.raises(kb.KvqError) as e:
             call(**kw)
         assert e.value.status == status, (kw, str(e.value))
+
+
+def test_mixed_rejected_before_launch(kb):
+    fake = 1 << 20
+    assert kb.kvq_mixed_sizes((2, 10, 128)) == (2 * 10 * 128 * 2, 2 * 11 * 8, 2 * 3)
+    for shape, x, off, status in (((2, 10, 96), fake, fake, kb.EUNSUPPORTED), ((2, 10, 128), None, fake, kb.EINVAL),
+                                  ((2, 10, 128), fake + 1, fake, kb.EINVAL), ((2, 10, 128), fake, fake + 4, kb.EINVAL)):
+        with pytest.raises(kb.KvqError) as e:
+            kb.kvq_mixed_quantize(x, fake, shape, fake, off, fake, 0)
+        assert e.value.status == status, (shape, str(e.value))
+    with pytest.raises(kb.KvqError) as e:
+        kb.kvq_mixed_dequantize(fake, fake, fake, (2, 10, 128), None, 0)
+    assert e.value.status == kb.EINVAL
 
