@@ -597,6 +597,24 @@ def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32,
     ms = med(decode_steps)
     out["2_kivi_int4/append_KV_one_token_us"] = round(1e3 * ms / 64, 2)
     del state, steps
+    # per-token mixed precision of the key cache, the four levels in equal shares
+    # (seeded tags): quantize reads K and writes the records, dequantize the reverse
+    shp = tuple(K.shape)
+    tags = torch.randint(0, 4, shp[:2], dtype=torch.uint8, device=dev, generator=torch.Generator(device=dev).manual_seed(4))
+    sB, oB, tB = b.kvq_mixed_sizes(shp)
+    mbuf = torch.empty(sB, dtype=torch.uint8, device=dev)
+    moff = torch.empty(oB // 8, dtype=torch.int64, device=dev)
+    mt2 = torch.empty(tB, dtype=torch.uint8, device=dev)
+    mout = torch.empty_like(K)
+    b.kvq_mixed_quantize(K, tags, shp, mbuf, moff, mt2, stream)
+    torch.cuda.synchronize()
+    used = int(moff.view(shp[0], shp[1] + 1)[:, -1].sum().item())      # record bytes of all slices
+    mq_B = K.numel() * 2 + tags.numel() + used + oB + tB
+    out["2_kivi_int4/K/mixed_quantize"] = entry(med(lambda: b.kvq_mixed_quantize(K, tags, shp, mbuf, moff, mt2, stream)), mq_B)
+    out["2_kivi_int4/K/mixed_dequantize"] = entry(med(lambda: b.kvq_mixed_dequantize(mbuf, moff, mt2, shp, mout, stream)),
+                                                  used + oB + tB + K.numel() * 2)
+    out["2_kivi_int4/K/mixed_bytes_per_number"] = round((used + tB) / K.numel(), 6)
+    del mbuf, moff, mt2, mout, tags
     # randomized Hadamard rotation of the key cache (bf16 -> bf16): read + write
     signs = torch.where(torch.rand(K.shape[-1], device=dev, generator=torch.Generator(device=dev).manual_seed(3)) < 0.5,
                         -1, 1).to(torch.int8)
