@@ -20,11 +20,13 @@
 // (channel c at bit (c mod 8/bits)*bits of byte c*bits/8, two's complement).
 #include <algorithm>
 
-#include "kvq_device.cuh"
+#include "kvq_elem.cuh"
 
 namespace kvq {
 
 namespace {
+
+using namespace elem;
 
 constexpr int kMThreads = 256;
 
@@ -82,106 +84,173 @@ __device__ __forceinline__ void put_bf16(uint8_t* p, float v) {
 }
 __device__ __forceinline__ float get_bf16(const uint8_t* p) { return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p)); }
 
-// Warp per token: E = C/32 consecutive channels per lane.
-template <int E>
+// 2-byte stores of a code word (records start at even offsets only)
+template <int BITS>
+__device__ __forceinline__ void store_word_u16(uint8_t* p, typename CodeWord<BITS>::T w) {
+    uint16_t* d = reinterpret_cast<uint16_t*>(p);
+    if constexpr (BITS == 2) {
+        d[0] = w;
+    } else if constexpr (BITS == 4) {
+        d[0] = (uint16_t)w;
+        d[1] = (uint16_t)(w >> 16);
+    } else {
+        d[0] = (uint16_t)w.x;
+        d[1] = (uint16_t)(w.x >> 16);
+        d[2] = (uint16_t)w.y;
+        d[3] = (uint16_t)(w.y >> 16);
+    }
+}
+template <int BITS>
+__device__ __forceinline__ typename CodeWord<BITS>::T load_word_u16(const uint8_t* p) {
+    const uint16_t* s = reinterpret_cast<const uint16_t*>(p);
+    if constexpr (BITS == 2) {
+        return s[0];
+    } else if constexpr (BITS == 4) {
+        return (uint32_t)s[0] | ((uint32_t)s[1] << 16);
+    } else {
+        return make_uint2((uint32_t)s[0] | ((uint32_t)s[1] << 16), (uint32_t)s[2] | ((uint32_t)s[3] << 16));
+    }
+}
+
+// Codes of one lane's 8 channels in the record's format, by the exact fast
+// quotient when the group allows it (the same constants and steps as the
+// uniform per-token kernels), else by the IEEE division.
+template <int BITS, bool ASYM>
+__device__ __forceinline__ void record_codes(const uint4& w, const GroupC& gc, const QSpec& q, uint8_t* pay) {
+    const int off = q.is_signed ? (1 << (BITS - 1)) : 0;
+    uint32_t cc[8];
+    if (gc.fast) {
+        QuotK kq[4];
+        kq[0].ns = pk(-gc.s, -gc.s);
+        kq[0].inv = pk(gc.inv, gc.inv);
+        kq[1] = kq[2] = kq[3] = kq[0];
+        int32_t zo[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) zo[j] = gc.zoff;
+        if (!ASYM || gc.lo_ok) codes8_fast<ASYM, false>(w, kq, zo, q.qmin + off, q.qmax + off, cc);
+        else codes8_fast<ASYM, true>(w, kq, zo, q.qmin + off, q.qmax + off, cc);
+    } else {
+        float s8[8], z8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { s8[j] = gc.s; z8[j] = gc.zp; }
+        codes8_slow<ASYM>(w, s8, z8, q, off, cc);
+    }
+    store_word_u16<BITS>(pay, finish_word<BITS>(cc, q.is_signed));
+}
+
+// LT = C/8 lanes per token, 8 channels (one 16-byte load) per lane; 32/LT
+// tokens per warp.  The token's min / max / abs-max are folded as bf16 pairs
+// and reduced over its LT lanes; the tag then selects the format.
+template <int LT>
 __global__ void __launch_bounds__(kMThreads)
 mixed_quant_kernel(const __nv_bfloat16* x, const uint8_t* tags, int64_t outer, int64_t T, const int64_t* off,
                    uint8_t* stream, const MixedFormats F)
 {
-    constexpr int C = 32 * E;
-    const int lane = threadIdx.x & 31;
+    constexpr int C = 8 * LT, TPW = 32 / LT;
+    const int lane = threadIdx.x & 31, sub = lane % LT;
     const uint64_t ntok = (uint64_t)outer * T;
     const uint64_t warps = (uint64_t)gridDim.x * (kMThreads / 32);
-    for (uint64_t w = (uint64_t)blockIdx.x * (kMThreads / 32) + (threadIdx.x >> 5); w < ntok; w += warps) {
-        const uint64_t o = w / T, t = w - o * T;
-        const int g = tags[w] & 3;
+    for (uint64_t w0 = ((uint64_t)blockIdx.x * (kMThreads / 32) + (threadIdx.x >> 5)) * TPW; w0 < ntok;
+         w0 += warps * TPW) {
+        const uint64_t tok = w0 + lane / LT;
+        const bool live = tok < ntok;
+        const uint4 v = live ? *reinterpret_cast<const uint4*>(x + tok * C + sub * 8) : make_uint4(0, 0, 0, 0);
+        uint32_t mn = kBfPosInf2, mx = kBfNegInf2, am = 0u;
+        fold_minmax(v, mn, mx);
+        fold_absmax(v, am);
+#pragma unroll
+        for (int d = 1; d < LT; d <<= 1) {
+            mn = bmin2(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, d));
+            mx = bmax2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, d));
+            am = bmax2(am, __shfl_xor_sync(0xFFFFFFFFu, am, d));
+        }
+        if (!live) continue;
+        const uint64_t o = tok / T, t = tok - o * T;
+        const int g = tags[tok] & 3;
         uint8_t* rec = stream + o * (uint64_t)T * 2 * C + off[o * (T + 1) + t];
-        float v[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[e] = __bfloat162float(x[w * C + lane * E + e]);
         if (g == 3) {                                              // 16 bits: the values as stored
+            uint16_t* d = reinterpret_cast<uint16_t*>(rec) + sub * 8;
+            const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int e = 0; e < E; ++e) put_bf16(rec + 2 * (lane * E + e), v[e]);
+            for (int k = 0; k < 4; ++k) { d[2 * k] = (uint16_t)ws[k]; d[2 * k + 1] = (uint16_t)(ws[k] >> 16); }
             continue;
         }
-        const QSpec& q = g == 0 ? F.f2 : (g == 1 ? F.f4 : F.f8);
-        const int bits = g == 0 ? 2 : (g == 1 ? 4 : 8);
-        float mn = v[0], mx = v[0], am = fabsf(v[0]);
-#pragma unroll
-        for (int e = 1; e < E; ++e) { mn = fminf(mn, v[e]); mx = fmaxf(mx, v[e]); am = fmaxf(am, fabsf(v[e])); }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, d));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, d));
-            am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, d));
+        const float fmn = fminf(lo_f(mn), hi_f(mn)), fmx = fmaxf(lo_f(mx), hi_f(mx)), fam = fmaxf(lo_f(am), hi_f(am));
+        GroupC gc;
+        int bits;
+        if (g == 2) {
+            gc = make_group<true>(fmn, fmx, F.f8, 0);
+            record_codes<8, true>(v, gc, F.f8, rec + sub * 8);
+            bits = 8;
+        } else if (g == 1) {
+            gc = make_group<false>(0.0f, fam, F.f4, 8);
+            record_codes<4, false>(v, gc, F.f4, rec + sub * 4);
+            bits = 4;
+        } else {
+            gc = make_group<false>(0.0f, fam, F.f2, 2);
+            record_codes<2, false>(v, gc, F.f2, rec + sub * 2);
+            bits = 2;
         }
-        const bool asym = g == 2;
-        const Meta m = asym ? meta_asym(mn, mx, q) : meta_sym(am, q);
-        const uint32_t mask = (1u << bits) - 1u;
-        // this lane's E codes occupy E*bits bits starting at bit lane*E*bits
-        uint32_t acc = 0;
-        int nb = 0;
-        uint8_t* pay = rec + (lane * E * bits) / 8;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int c = asym ? quant_code<true>(v[e], m, q.lo, q.hi) : quant_code<false>(v[e], m, q.lo, q.hi);
-            acc |= ((uint32_t)c & mask) << nb;
-            nb += bits;
-            if (nb == 8) { *pay++ = (uint8_t)acc; acc = 0; nb = 0; }
-        }
-        if (nb) {                                                  // 2-bit codes of fewer than 4 channels
-            // the lane's bits share a byte with the next lane's: combine within the warp
-            const uint32_t mine = acc;
-            const int lanes_per_byte = 8 / (E * bits);
-            uint32_t b = 0;
-            const int first = lane - lane % lanes_per_byte;
-            for (int j = 0; j < lanes_per_byte; ++j)
-                b |= __shfl_sync(0xFFFFFFFFu, mine, first + j) << (j * E * bits);
-            if (lane % lanes_per_byte == 0) *pay = (uint8_t)b;
-        }
-        if (lane == 0) {
+        if (sub == 0) {
             const int64_t pb = (int64_t)C * bits / 8;
-            put_bf16(rec + pb, m.s);
-            if (asym) put_bf16(rec + pb + 2, m.z);
+            put_bf16(rec + pb, gc.s);
+            if (g == 2) put_bf16(rec + pb + 2, gc.zp);
         }
     }
 }
 
-template <int E>
+// LT lanes per token, 8 channels per lane, one 16-byte store each.
+template <int LT>
 __global__ void __launch_bounds__(kMThreads)
 mixed_dequant_kernel(const uint8_t* stream, const uint8_t* tags2, int64_t outer, int64_t T, const int64_t* off,
                      __nv_bfloat16* out)
 {
-    constexpr int C = 32 * E;
-    const int lane = threadIdx.x & 31;
+    constexpr int C = 8 * LT, TPW = 32 / LT;
+    const int lane = threadIdx.x & 31, sub = lane % LT;
     const uint64_t ntok = (uint64_t)outer * T;
     const uint64_t warps = (uint64_t)gridDim.x * (kMThreads / 32);
     const int64_t tb = (T + 3) / 4;
-    for (uint64_t w = (uint64_t)blockIdx.x * (kMThreads / 32) + (threadIdx.x >> 5); w < ntok; w += warps) {
-        const uint64_t o = w / T, t = w - o * T;
+    for (uint64_t w0 = ((uint64_t)blockIdx.x * (kMThreads / 32) + (threadIdx.x >> 5)) * TPW; w0 < ntok;
+         w0 += warps * TPW) {
+        const uint64_t tok = w0 + lane / LT;
+        if (tok >= ntok) continue;
+        const uint64_t o = tok / T, t = tok - o * T;
         const int g = (tags2[o * tb + t / 4] >> (2 * (t % 4))) & 3;
         const uint8_t* rec = stream + o * (uint64_t)T * 2 * C + off[o * (T + 1) + t];
-        __nv_bfloat16* dst = out + w * C + lane * E;
+        uint4 r;
         if (g == 3) {
+            const uint16_t* sv = reinterpret_cast<const uint16_t*>(rec) + sub * 8;
+            r = make_uint4((uint32_t)sv[0] | ((uint32_t)sv[1] << 16), (uint32_t)sv[2] | ((uint32_t)sv[3] << 16),
+                           (uint32_t)sv[4] | ((uint32_t)sv[5] << 16), (uint32_t)sv[6] | ((uint32_t)sv[7] << 16));
+        } else {
+            const int bits = g == 0 ? 2 : (g == 1 ? 4 : 8);
+            const int64_t pb = (int64_t)C * bits / 8;
+            Meta m;
+            m.s = get_bf16(rec + pb);
+            m.z = g == 2 ? get_bf16(rec + pb + 2) : 0.0f;
+            uint32_t u[8];
+            if (g == 2) unpack_biased8<8>(load_word_u16<8>(rec + sub * 8), u);
+            else if (g == 1) unpack_biased8<4>(flip_signs<4>(load_word_u16<4>(rec + sub * 4)), u);
+            else unpack_biased8<2>(flip_signs<2>(load_word_u16<2>(rec + sub * 2)), u);
+            const int offb = g == 2 ? 0 : (1 << (bits - 1));   // offset binary of the symmetric codes
+            u64 cp[4], sp[4];
+            bool fast;
+            u64 cph, sph;
+            dq_consts(m.s, m.z, offb, cph, sph, fast);
 #pragma unroll
-            for (int e = 0; e < E; ++e) dst[e] = __float2bfloat16_rn(get_bf16(rec + 2 * (lane * E + e)));
-            continue;
-        }
-        const int bits = g == 0 ? 2 : (g == 1 ? 4 : 8);
-        const int64_t pb = (int64_t)C * bits / 8;
-        Meta m;
-        m.s = get_bf16(rec + pb);
-        m.z = g == 2 ? get_bf16(rec + pb + 2) : 0.0f;
-        const uint32_t mask = (1u << bits) - 1u;
+            for (int k = 0; k < 4; ++k) { cp[k] = cph; sp[k] = sph; }
+            TileAcc ta;
+            uint32_t mxb = 0;
+            if (fast) {
+                r = dq8<false>(u, cp, sp, make_uint4(0, 0, 0, 0), ta, mxb);
+            } else {
+                float zs[8], ss[8];
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int c = lane * E + e;
-            const uint32_t byte = rec[(c * bits) / 8];
-            uint32_t f = (byte >> ((c * bits) % 8)) & mask;
-            int qv = (int)f;
-            if (g != 2 && (f >> (bits - 1))) qv -= (1 << bits);    // symmetric: two's complement
-            dst[e] = __float2bfloat16_rn(dequant_value(qv, m));
+                for (int j = 0; j < 8; ++j) { zs[j] = m.z; ss[j] = m.s; }
+                r = dq8_slow<false>(u, offb, zs, ss, make_uint4(0, 0, 0, 0), ta, mxb);
+            }
         }
+        *reinterpret_cast<uint4*>(out + tok * C + sub * 8) = r;
     }
 }
 
@@ -206,9 +275,9 @@ cudaError_t launch_mixed_quantize(const void* x, const uint8_t* tags, int64_t ou
     uint8_t* sb = static_cast<uint8_t*>(stream_buf);
     const unsigned grid = warps_grid((uint64_t)outer * T);
     switch (C) {
-    case 64: mixed_quant_kernel<2><<<grid, kMThreads, 0, st>>>(xb, tags, outer, T, off, sb, F); break;
-    case 128: mixed_quant_kernel<4><<<grid, kMThreads, 0, st>>>(xb, tags, outer, T, off, sb, F); break;
-    default: mixed_quant_kernel<8><<<grid, kMThreads, 0, st>>>(xb, tags, outer, T, off, sb, F); break;
+    case 64: mixed_quant_kernel<8><<<grid, kMThreads, 0, st>>>(xb, tags, outer, T, off, sb, F); break;
+    case 128: mixed_quant_kernel<16><<<grid, kMThreads, 0, st>>>(xb, tags, outer, T, off, sb, F); break;
+    default: mixed_quant_kernel<32><<<grid, kMThreads, 0, st>>>(xb, tags, outer, T, off, sb, F); break;
     }
     return cudaGetLastError();
 }
@@ -221,9 +290,9 @@ cudaError_t launch_mixed_dequantize(const void* stream_buf, const int64_t* off, 
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
     const unsigned grid = warps_grid((uint64_t)outer * T);
     switch (C) {
-    case 64: mixed_dequant_kernel<2><<<grid, kMThreads, 0, st>>>(sb, tags2, outer, T, off, ob); break;
-    case 128: mixed_dequant_kernel<4><<<grid, kMThreads, 0, st>>>(sb, tags2, outer, T, off, ob); break;
-    default: mixed_dequant_kernel<8><<<grid, kMThreads, 0, st>>>(sb, tags2, outer, T, off, ob); break;
+    case 64: mixed_dequant_kernel<8><<<grid, kMThreads, 0, st>>>(sb, tags2, outer, T, off, ob); break;
+    case 128: mixed_dequant_kernel<16><<<grid, kMThreads, 0, st>>>(sb, tags2, outer, T, off, ob); break;
+    default: mixed_dequant_kernel<32><<<grid, kMThreads, 0, st>>>(sb, tags2, outer, T, off, ob); break;
     }
     return cudaGetLastError();
 }
