@@ -35,45 +35,49 @@ __host__ __device__ __forceinline__ int64_t record_bytes(int g, int64_t C) {
     return g == 0 ? C / 4 + 2 : g == 1 ? C / 2 + 2 : g == 2 ? C + 4 : 2 * C;
 }
 
-// One CTA per slice: record offsets by a block-wide exclusive scan over the
-// tokens (chunks of kMThreads), and the packed 2-bit tags.
+// One CTA per slice.  Thread i owns the tokens [i*K, (i+1)*K), K = ceil(T /
+// 256) rounded up to a multiple of 4: it sums its records' sizes, the block
+// scans the 256 sums, and each thread then writes its tokens' offsets and the
+// bytes of packed tags that cover them (no byte is shared by two threads).
 __global__ void __launch_bounds__(kMThreads)
 mixed_plan_kernel(const uint8_t* tags, int64_t T, int64_t C, int64_t* off, uint8_t* tags2)
 {
     __shared__ int64_t warp_sums[kMThreads / 32];
-    __shared__ int64_t carry;
     const int64_t o = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint8_t* tg = tags + o * T;
     int64_t* of = off + o * (T + 1);
-    if (tid == 0) carry = 0;
-    __syncthreads();
-    for (int64_t base = 0; base < T; base += kMThreads) {
-        const int64_t t = base + tid;
-        const int64_t sz = t < T ? record_bytes(tg[t] & 3, C) : 0;
-        int64_t v = sz;                                            // inclusive scan within the warp
+    uint8_t* t2 = tags2 + o * ((T + 3) / 4);
+    const int64_t K = ((T + kMThreads - 1) / kMThreads + 3) / 4 * 4;
+    const int64_t t0 = std::min<int64_t>(T, (int64_t)tid * K), t1 = std::min<int64_t>(T, t0 + K);
+    int64_t sum = 0;
+#pragma unroll 8
+    for (int64_t t = t0; t < t1; ++t) sum += record_bytes(tg[t] & 3, C);
+    int64_t v = sum;                                               // inclusive scan within the warp
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int64_t u = __shfl_up_sync(0xFFFFFFFFu, v, d);
-            if (lane >= d) v += u;
-        }
-        if (lane == 31) warp_sums[warp] = v;
-        __syncthreads();
-        int64_t before = carry;
-        for (int w = 0; w < warp; ++w) before += warp_sums[w];
-        if (t < T) of[t] = before + v - sz;
-        __syncthreads();
-        if (tid == kMThreads - 1) carry = before + v;             // the chunk's total
-        __syncthreads();
+    for (int d = 1; d < 32; d <<= 1) {
+        const int64_t u = __shfl_up_sync(0xFFFFFFFFu, v, d);
+        if (lane >= d) v += u;
     }
-    if (tid == 0) of[T] = carry;
-    // packed tags: thread handles one byte (4 tokens)
-    for (int64_t k = tid; k < (T + 3) / 4; k += kMThreads) {
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    int64_t before = 0;
+    for (int w = 0; w < warp; ++w) before += warp_sums[w];
+    int64_t run = before + v - sum;                                // offset of token t0
+    for (int64_t t = t0; t < t1; t += 4) {
         uint32_t b = 0;
-        for (int j = 0; j < 4; ++j)
-            if (k * 4 + j < T) b |= (uint32_t)(tg[k * 4 + j] & 3) << (2 * j);
-        tags2[o * ((T + 3) / 4) + k] = (uint8_t)b;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (t + j < t1) {
+                const int g = tg[t + j] & 3;
+                of[t + j] = run;
+                run += record_bytes(g, C);
+                b |= (uint32_t)g << (2 * j);
+            }
+        }
+        t2[t / 4] = (uint8_t)b;
     }
+    if (tid == kMThreads - 1) of[T] = before + v;                  // the slice's total
 }
 
 struct MixedFormats { QSpec f2, f4, f8; };                         // per-token formats of tags 0, 1, 2

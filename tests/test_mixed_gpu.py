@@ -58,7 +58,27 @@ def expected(X, tags):
     return streams, offs, t2, deq
 
 
-def run(b, shape, tags, kind="normal", seed=0):
+def expected_one_level(X, tag):
+    """expected() for a cache whose tokens all carry one tag below 3, from whole-
+    tensor oracle calls: per-token groups give one record per token row."""
+    outer, T, C = X.shape
+    qp = formats(C)[tag]
+    q = O.quantize(X, O.BF16, qp)
+    parts = [q.codes.reshape(outer, T, -1), q.scale.view(np.uint8).reshape(outer, T, -1)]
+    if q.zero.size:
+        parts.append(q.zero.view(np.uint8).reshape(outer, T, -1))
+    recs = np.concatenate(parts, axis=2)
+    rb = recs.shape[2]
+    offs = np.tile(np.arange(T + 1, dtype=np.int64) * rb, (outer, 1))
+    streams = [recs[o].tobytes() for o in range(outer)]
+    t2 = np.zeros((outer, (T + 3) // 4), np.uint8)
+    for j in range(4):
+        t2[:, : (T - j + 3) // 4] |= np.uint8(tag << (2 * j))
+    deq = O.dequantize(q, X.shape, qp, O.BF16).reshape(X.shape)
+    return streams, offs, t2, deq
+
+
+def run(b, shape, tags, kind="normal", seed=0, one_level=None):
     import torch
     outer, T, C = shape
     rng = np.random.default_rng(seed)
@@ -80,7 +100,7 @@ def run(b, shape, tags, kind="normal", seed=0):
     b.kvq_mixed_quantize(xd, td, shape, sbuf, off, t2)
     b.kvq_mixed_dequantize(sbuf, off, t2, shape, out)
     torch.cuda.synchronize()
-    streams, offs, t2w, deq = expected(X, tags)
+    streams, offs, t2w, deq = expected(X, tags) if one_level is None else expected_one_level(X, one_level)
     got_off = off.cpu().numpy().reshape(outer, T + 1)
     assert np.array_equal(got_off, offs), "record offsets differ"
     assert np.array_equal(t2.cpu().numpy().reshape(outer, -1), t2w), "packed tags differ"
@@ -95,6 +115,23 @@ def test_mixed_random_tags(b, C):
     rng = np.random.default_rng(C)
     shape = (2, 301, C)
     run(b, shape, rng.integers(0, 4, shape[:2]), seed=zlib.crc32(repr(C).encode()))
+
+
+def test_mixed_random_tags_long_slices(b):
+    """Thousands of tokens per slice: each thread of the offset scan sums a
+    segment of 20 tokens, the last one ragged (5003 = 250 * 20 + 3)."""
+    rng = np.random.default_rng(5003)
+    shape = (2, 5003, 64)
+    run(b, shape, rng.integers(0, 4, shape[:2]), seed=11)
+
+
+@pytest.mark.parametrize("tag", [0, 1, 2])
+def test_mixed_one_level_beyond_one_grid_pass(b, tag):
+    """More token rows than one pass of the capped grid covers, so every warp
+    loops; a 784-token scan segment per thread with a ragged end."""
+    T = 200003
+    shape = (1, T, 128)
+    run(b, shape, np.full(shape[:2], tag), seed=tag + 20, one_level=tag)
 
 
 @pytest.mark.parametrize("tag", [0, 1, 2, 3])
