@@ -146,3 +146,37 @@ def test_attend_empty_outer(b):
     kq, vq = kq_of(b, KIVI_K), kq_of(b, KIVI_V)
     b.kvq_attend_decode(q, 1, e, e, e, e, kq, e, e, e, e, vq, shape, out, e, 16)
     torch.cuda.synchronize()
+
+
+def test_attend_output_shift_within_value_error_bound(b):
+    """The value bound of "KV cache 压缩：把历史装得更小" §"K 的误差会改变权重，V 的误差会改变
+    内容" on the kernel: with the same quantized keys on both sides the weights
+    agree, so y_gpu(K^, V^) - y(K^, V) = sum_i a_i dv_i up to the kernel's own
+    float32 error, and its norm is at most max_i ||dv_i|| plus the norm of the
+    derived tolerance.  The full KIVI workload, one query per KV head."""
+    import torch
+    shape = (64, 8192, 128)
+    rng = np.random.default_rng(77)
+    xk = W.to_bf16_bits(W.random_kv(rng, shape))
+    xv = W.to_bf16_bits(W.random_kv(rng, shape))
+    q = rng.standard_normal((shape[0], 1, shape[2])).astype(np.float32)
+    qk, qv = O.quantize(xk, O.BF16, KIVI_K), O.quantize(xv, O.BF16, KIVI_V)
+    K = O.dequantize_f64(qk, shape, KIVI_K, O.BF16)
+    Vh = O.dequantize_f64(qv, shape, KIVI_V, O.BF16)
+    V = O.bf16_bits_to_f32(xv).astype(np.float64)
+    y_exact_v = O.attend(q.astype(np.float64), K, V)
+
+    dk, dv = upload(qk), upload(qv)
+    qd = torch.from_numpy(q).cuda()
+    out = torch.full((shape[0], 1, shape[2]), float("nan"), dtype=torch.float32, device="cuda")
+    wB = b.kvq_attend_workspace(shape, 1)
+    ws = torch.empty(max(wB, 1), dtype=torch.uint8, device="cuda")
+    b.kvq_attend_decode(qd, 1, *dk, kq_of(b, KIVI_K), *dv, kq_of(b, KIVI_V), shape, out, ws, wB)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    tol = bound(q.astype(np.float64), K, Vh, splits=-(-shape[1] // 256))
+    dy = np.linalg.norm(got - y_exact_v, axis=-1)                       # [O, 1]
+    dv_max = np.linalg.norm(Vh - V, axis=-1).max(axis=1)[:, None]       # [O, 1]
+    assert np.all(np.isfinite(got))
+    assert np.all(dy <= dv_max + np.linalg.norm(tol, axis=-1)), f"worst ratio {(dy / dv_max).max():.3f}"
+    assert dy.max() > 0
