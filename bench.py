@@ -465,6 +465,7 @@ def run_ours(args, rank, world, local_rank):
                          "bytes_per_launch": sel_B, "traffic": ncu_traffic()},
             "ms_per_step_rows_in_sequence": round(serial_ms, 5) if serial_ms else None,
             "gpu_launches": launches,
+            "wait_timeouts": b.kvq_wait_timeouts(),    # bounded waits that gave up in this process: 0
             "wall_s_timed_region": round(wall, 3),
             "clocks": clk.summary(),
         }

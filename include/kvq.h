@@ -344,6 +344,16 @@ KVQ_API kvq_status kvq_error_stats_noalloc(const void* x, kvq_dtype x_dtype, con
                                            const kvq_shape* shape, const kvq_qparams* p, kvq_err* out_dev,
                                            void* stream);
 
+/* Bounded waits that gave up.  Every wait of the library's kernels on a copy
+ * or a peer CTA (an mbarrier phase, a cluster barrier) polls a bounded number
+ * of times; a wait that runs out records itself in a device counter and the
+ * kernel returns early, so its outputs are undefined.  This call synchronises
+ * the current device (all streams), then writes to *count the number of such
+ * waits since the library was loaded, over all kernels.  0 is the only value a
+ * correct run produces.  Host pointer; KVQ_EINVAL if NULL, KVQ_ECUDA if the
+ * synchronisation reports an error. */
+KVQ_API kvq_status kvq_wait_timeouts(uint64_t* count);
+
 /* Message describing the last non-OK status returned on this thread. */
 KVQ_API const char* kvq_last_error(void);
 

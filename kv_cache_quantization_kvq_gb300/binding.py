@@ -73,6 +73,7 @@ def _load() -> ctypes.CDLL:
         "kvq_mixed_sizes": [S, psz, psz, psz],
         "kvq_mixed_quantize": [vp, vp, S, vp, vp, vp, vp],
         "kvq_mixed_dequantize": [vp, vp, vp, S, vp, vp],
+        "kvq_wait_timeouts": [ctypes.POINTER(ctypes.c_uint64)],
         "kvq_append": [vp, i64, i32, S, P, i64, vp, vp, vp, vp, ctypes.POINTER(i64), ctypes.POINTER(i64), vp, sz,
                        vp],
     }
@@ -94,7 +95,8 @@ EXPORTS = ("kvq_quantized_sizes", "kvq_quantize", "kvq_dequantize", "kvq_error_s
            "kvq_compression_ratio", "kvq_token_compression_ratio", "kv_select_workspace",
            "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kv_compact_kv", "kvq_last_error", "kvq_version",
            "kvq_error_stats_noalloc", "kvq_attend_workspace", "kvq_attend_decode", "kvq_rotate",
-           "kvq_append_workspace", "kvq_append", "kvq_mixed_sizes", "kvq_mixed_quantize", "kvq_mixed_dequantize")
+           "kvq_append_workspace", "kvq_append", "kvq_mixed_sizes", "kvq_mixed_quantize", "kvq_mixed_dequantize",
+           "kvq_wait_timeouts")
 
 # size of the library's fixed scratch array behind kvq_error_stats_noalloc
 NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -158,6 +160,14 @@ def _shape(shape) -> kvq_shape:
 
 def kvq_version() -> str:
     return LIB.kvq_version().decode()
+
+
+def kvq_wait_timeouts() -> int:
+    """Bounded waits of the library's kernels that gave up since it was loaded
+    (synchronises the device); 0 in every correct run."""
+    n = ctypes.c_uint64()
+    _check(LIB.kvq_wait_timeouts(ctypes.byref(n)))
+    return int(n.value)
 
 
 def kvq_quantized_sizes(shape, x_dtype: int, qp: QParams):

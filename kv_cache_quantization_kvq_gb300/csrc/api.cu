@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <string>
+#include <vector>
 
 #include "kvq_internal.h"
 
@@ -185,6 +186,16 @@ int sm_count()
     return cache[dev];
 }
 
+// Readers of the per-translation-unit bounded-wait counters (kvq_bulk.cuh),
+// filled during static initialisation of the library.
+std::vector<unsigned int (*)()>& wait_counters()
+{
+    static std::vector<unsigned int (*)()> v;
+    return v;
+}
+
+void register_wait_counter(unsigned int (*read)()) { wait_counters().push_back(read); }
+
 }  // namespace kvq
 
 extern "C" {
@@ -192,6 +203,17 @@ extern "C" {
 const char* kvq_last_error(void) { return g_last_error.c_str(); }
 
 const char* kvq_version(void) { return "kvq 0.1.0 (sm_103a)"; }
+
+kvq_status kvq_wait_timeouts(uint64_t* count)
+{
+    if (!count) return fail(KVQ_EINVAL, "count must not be NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(KVQ_ECUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+    uint64_t n = 0;
+    for (auto* read : kvq::wait_counters()) n += read();
+    *count = n;
+    return KVQ_OK;
+}
 
 kvq_status kvq_quantized_sizes(const kvq_shape* shape, kvq_dtype x_dtype, const kvq_qparams* p,
                                size_t* codes_B, size_t* scale_B, size_t* zero_B, size_t* resid_B,

@@ -14,6 +14,19 @@ namespace kvq {
 // per translation unit that includes this header.
 static __device__ unsigned int g_kvq_wait_timeouts;
 
+// Host side: every translation unit that includes this header registers a
+// reader of its own counter at load time; kvq_wait_timeouts() sums them.
+void register_wait_counter(unsigned int (*read)());
+
+namespace {
+unsigned int read_wait_timeouts_of_this_unit()
+{
+    unsigned int v = 0;
+    return cudaMemcpyFromSymbol(&v, g_kvq_wait_timeouts, sizeof v) == cudaSuccess ? v : 0u;
+}
+const bool g_wait_counter_registered = (register_wait_counter(&read_wait_timeouts_of_this_unit), true);
+}  // namespace
+
 constexpr uint32_t kWaitLimit = 1u << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

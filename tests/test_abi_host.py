@@ -33,7 +33,7 @@ def declared_symbols():
 
 def test_library_exports_every_declared_symbol(kb):
     declared = declared_symbols()
-    assert len(declared) == 22
+    assert len(declared) == 23
     for name in declared:
         assert hasattr(kb.LIB, name), name
     assert declared == set(kb.EXPORTS)
@@ -198,6 +198,12 @@ def test_misaligned_buffers_rejected(kb):
         kb.kv_h2o_select(base, 2, 4, 64, 8, 2, base, None, base + 8, ws, 0)
     with pytest.raises(kb.KvqError):
         kb.kv_compact(base, kb.BF16, 2, 64, 8, base + 1, 4, base, 0)
+
+
+def test_wait_timeouts_rejects_null(kb):
+    """Argument checks run before the device synchronisation: no GPU needed."""
+    assert kb.LIB.kvq_wait_timeouts(None) == kb.EINVAL
+    assert "count" in kb.LIB.kvq_last_error().decode()
 
 
 def test_attend_rejected_before_launch(kb):

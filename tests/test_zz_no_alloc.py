@@ -5,8 +5,9 @@ synchronise the device).  It uses the library's fixed scratch array instead
 of a workspace; its results must match kvq_error_stats given a workspace, on
 two calls in a row (the array keeps the previous call's contents).
 
-This file is collected last so that a run stopping at the first failure has
-already run every other test; it also passes on its own in a fresh process.
+This file is collected after every other parity test (only the wait-timeout
+check follows), so that a run stopping at the first failure has already run
+them; it also passes on its own in a fresh process.
 """
 import numpy as np
 import pytest
