@@ -23,8 +23,12 @@
  *  - Ownership: every buffer pointer is a DEVICE pointer owned by the caller,
  *    except the small descriptor structs (kvq_shape, kvq_qparams), which are
  *    read on the host during the call and may be freed when it returns.  The
- *    library never allocates, frees or synchronises; sizes of every output
- *    and workspace come from kvq_quantized_sizes / kv_select_workspace.
+ *    library never allocates, frees or synchronises (the one exception is the
+ *    diagnostic kvq_wait_timeouts, which synchronises the device); sizes of
+ *    every output and workspace come from the size and workspace queries
+ *    (kvq_quantized_sizes, kv_select_workspace, kvq_attend_workspace,
+ *    kvq_append_workspace, kvq_mixed_sizes).  Host pointers, where an entry
+ *    point takes one, say so in its comment.
  *  - Asynchrony: device work is enqueued on `stream`; outputs are valid once
  *    the stream reaches that point.  Workspace contents are scratch and must
  *    not be shared by calls that may overlap on the GPU.
