@@ -69,3 +69,13 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_all_cores_oracle_baseline_spawns_independent_processes():
+    """The all-cores CPU baseline: spawned processes, each on its own slice;
+    its bytes per second add up over the processes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    d = bench.cpu_baseline_all_cores(min_seconds=0.3, processes=2)
+    assert d["kind"] == "oracle" and d["cores"] == 2 and d["value"] > 0
+    assert "2 processes" in d["sample"]
