@@ -774,11 +774,17 @@ def cpu_baseline_all_cores(min_seconds=10.0, processes=None):
     own KIVI slice and eviction head -- for about min_seconds.  GB/s = the
     algorithmic bytes of all processes / the longest process's loop time."""
     import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
     import oracle as O
     O.build()
     n = processes or (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
-    with mp.get_context("spawn").Pool(n) as pool:
-        res = pool.map(_oracle_worker, [(100 + i, min_seconds) for i in range(n)])
+    # a worker that dies raises BrokenProcessPool instead of blocking; every wait is bounded
+    ex = ProcessPoolExecutor(max_workers=n, mp_context=mp.get_context("spawn"))
+    try:
+        futs = [ex.submit(_oracle_worker, (100 + i, min_seconds)) for i in range(n)]
+        res = [f.result(timeout=10 * min_seconds + 300) for f in futs]
+    finally:
+        ex.shutdown(wait=False, cancel_futures=True)
     nbytes, el, done = sum(r[0] for r in res), max(r[1] for r in res), sum(r[2] for r in res)
     return {"value": round(nbytes / el / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
             "sample": f"{n} processes of the one-core sample, each on its own KIVI slice and eviction head; "
