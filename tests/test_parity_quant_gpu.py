@@ -177,13 +177,12 @@ def test_along_t_fast(b, case):
 
 
 # Long groups along T (one scale per channel over hundreds to thousands of
-# tokens): bf16 sources take the cluster kernel, where 1 to 16 CTAs share one
+# tokens), bf16 sources: the cluster kernel, where 1 to 16 CTAs share one
 # group of 64 channels (ceil(group / 512) CTAs, or ceil(group / 1024) where
-# clusters of 16 are unavailable) and persistent clusters walk the units
-# through a ring of shared-memory slots; groups beyond 8192 tokens take the
-# two-pass path.  Ragged last groups (some CTAs of a cluster get no rows),
-# residual windows, several channel blocks, and (last two) many more units
-# than resident clusters, so every ring slot is refilled several times.
+# clusters of 16 cannot be resident), one cluster per unit; groups beyond 8192
+# tokens take the two-pass path through the workspace.  Ragged last groups
+# (some CTAs of a cluster get no rows), residual windows, several channel
+# blocks, and many more units than resident clusters.
 LONG_T_CASES = [
     # bits, mode (qmin, qmax) or None, g, T, R, C, kind, outer
     (8, None, 0, 4100, 4, 128, "normal", 2),
