@@ -348,7 +348,8 @@ KVQ_API kvq_status kvq_error_stats_noalloc(const void* x, kvq_dtype x_dtype, con
                                            const kvq_shape* shape, const kvq_qparams* p, kvq_err* out_dev,
                                            void* stream);
 
-/* Bounded waits that gave up.  Every wait of the library's kernels on a copy
+/* Bounded waits that gave up (a diagnostic of this library; no counterpart on
+ * the pages).  Every wait of the library's kernels on a copy
  * or a peer CTA (an mbarrier phase, a cluster barrier) polls a bounded number
  * of times; a wait that runs out records itself in a device counter and the
  * kernel returns early, so its outputs are undefined.  This call synchronises
