@@ -349,10 +349,12 @@ KVQ_API kvq_status kvq_error_stats_noalloc(const void* x, kvq_dtype x_dtype, con
                                            void* stream);
 
 /* Bounded waits that gave up (a diagnostic of this library; no counterpart on
- * the pages).  Every wait of the library's kernels on a copy
- * or a peer CTA (an mbarrier phase, a cluster barrier) polls a bounded number
- * of times; a wait that runs out records itself in a device counter and the
- * kernel returns early, so its outputs are undefined.  This call synchronises
+ * the pages).  Every wait of the library's kernels on an asynchronous copy
+ * (an mbarrier phase) polls a bounded number of times; a wait that runs out
+ * records itself in a device counter and the kernel leaves its loop, so its
+ * outputs are undefined.  (The cluster kernels' barriers are hardware cluster
+ * barriers that every CTA of the cluster reaches on every path, timeouts
+ * included.)  This call synchronises
  * the current device (all streams), then writes to *count the number of such
  * waits since the library was loaded, over all kernels.  0 is the only value a
  * correct run produces.  Host pointer; KVQ_EINVAL if NULL, KVQ_ECUDA if the

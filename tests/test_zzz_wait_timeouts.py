@@ -1,9 +1,9 @@
 """No bounded wait of the library's kernels gave up (kvq_wait_timeouts).
 
-Every wait of the staged, warp-specialised and cluster kernels on a bulk copy
-or a peer CTA polls a bounded number of times; one that runs out records
-itself in a device counter and its kernel returns early, leaving its outputs
-undefined.  Collected after every other test, so in a full run the count
+Every wait of the staged, warp-specialised and cluster kernels on an
+asynchronous copy (an mbarrier phase) polls a bounded number of times; one that
+runs out records itself in a device counter and its kernel leaves its loop,
+leaving its outputs undefined.  Collected after every other test, so in a full run the count
 covers the whole suite; it first runs each kernel family with bounded waits
 once, so that it also means something on its own.
 """
