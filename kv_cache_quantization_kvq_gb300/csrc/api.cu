@@ -7,6 +7,8 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -175,26 +177,56 @@ void set_last_error(const char* fmt, ...)
 
 int sm_count()
 {
-    static int cache[128] = {0};
+    static std::atomic<int> cache[128];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
-    if (cache[dev] == 0) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n > 0 ? n : 148;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 148;
+        }
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
+}
+
+cudaError_t ensure_kernel_attrs(const void* fn, int smem_bytes, bool nonportable_cluster)
+{
+    struct Entry { const void* fn; int dev; int smem; bool npc; };
+    static std::mutex mu;
+    static std::vector<Entry> table;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry* hit = nullptr;
+    for (Entry& t : table)
+        if (t.fn == fn && t.dev == dev) { hit = &t; break; }
+    if (hit && hit->smem >= smem_bytes && (hit->npc || !nonportable_cluster)) return cudaSuccess;
+    const int want = hit ? std::max(hit->smem, smem_bytes) : smem_bytes;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (e == cudaSuccess && nonportable_cluster)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;      // also the thread's last error: the launch path reports it
+    if (hit) {
+        hit->smem = want;
+        hit->npc = hit->npc || nonportable_cluster;
+    } else {
+        table.push_back(Entry{fn, dev, want, nonportable_cluster});
+    }
+    return cudaSuccess;
 }
 
 // Readers of the per-translation-unit bounded-wait counters (kvq_bulk.cuh),
 // filled during static initialisation of the library.
-std::vector<unsigned int (*)()>& wait_counters()
+std::vector<cudaError_t (*)(unsigned int*)>& wait_counters()
 {
-    static std::vector<unsigned int (*)()> v;
+    static std::vector<cudaError_t (*)(unsigned int*)> v;
     return v;
 }
 
-void register_wait_counter(unsigned int (*read)()) { wait_counters().push_back(read); }
+void register_wait_counter(cudaError_t (*read)(unsigned int*)) { wait_counters().push_back(read); }
 
 }  // namespace kvq
 
@@ -210,7 +242,12 @@ kvq_status kvq_wait_timeouts(uint64_t* count)
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail(KVQ_ECUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
     uint64_t n = 0;
-    for (auto* read : kvq::wait_counters()) n += read();
+    for (auto* read : kvq::wait_counters()) {
+        unsigned int v = 0;
+        e = read(&v);
+        if (e != cudaSuccess) return fail(KVQ_ECUDA, "reading a bounded-wait counter: %s", cudaGetErrorString(e));
+        n += v;
+    }
     *count = n;
     return KVQ_OK;
 }

@@ -322,13 +322,10 @@ template <int BITS, bool ASYM>
 bool wq_l_launch(const QArgs& a, cudaStream_t st) {
     const QSpec& q = a.q;
     auto kernel = wq_l_kernel<BITS, ASYM>;
-    static const bool attr = [] {
-        cudaFuncSetAttribute(wq_l_kernel<BITS, ASYM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLSmemCap);
-        cudaFuncSetAttribute(wq_l_kernel<BITS, ASYM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        cudaGetLastError();
-        return true;
-    }();
-    (void)attr;
+    if (ensure_kernel_attrs(reinterpret_cast<const void*>(kernel), (int)kLSmemCap, true) != cudaSuccess) {
+        cudaGetLastError();          // not handled here: the caller takes the two-pass path
+        return false;
+    }
     // 512-row slices (64 KB: three CTAs per SM) and up to 16 CTAs per
     // cluster; where 16-CTA clusters cannot be resident, 1024-row slices and
     // up to 8 CTAs

@@ -15,14 +15,15 @@ namespace kvq {
 static __device__ unsigned int g_kvq_wait_timeouts;
 
 // Host side: every translation unit that includes this header registers a
-// reader of its own counter at load time; kvq_wait_timeouts() sums them.
-void register_wait_counter(unsigned int (*read)());
+// reader of its own counter at load time; kvq_wait_timeouts() sums them.  A
+// reader returns the error of the copy (its value is then not meaningful).
+void register_wait_counter(cudaError_t (*read)(unsigned int*));
 
 namespace {
-unsigned int read_wait_timeouts_of_this_unit()
+cudaError_t read_wait_timeouts_of_this_unit(unsigned int* v)
 {
-    unsigned int v = 0;
-    return cudaMemcpyFromSymbol(&v, g_kvq_wait_timeouts, sizeof v) == cudaSuccess ? v : 0u;
+    *v = 0u;
+    return cudaMemcpyFromSymbol(v, g_kvq_wait_timeouts, sizeof *v);
 }
 const bool g_wait_counter_registered = (register_wait_counter(&read_wait_timeouts_of_this_unit), true);
 }  // namespace

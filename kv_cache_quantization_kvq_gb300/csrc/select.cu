@@ -867,22 +867,17 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st)
             const int64_t per_part = (rs + kGFParts - 1) / kGFParts;
             const int jpt = (int)std::max<int64_t>(1, (per_part + 4 * kFinThreads - 1) / (4 * kFinThreads));
             if (jpt <= kGFMaxJ && vec && T >= 4) {
-                static size_t attr_gf = 0;
-                if (smem > attr_gf) {
-                    cudaFuncSetAttribute(gather_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                    attr_gf = smem;
-                }
+                cudaError_t ea = ensure_kernel_attrs(reinterpret_cast<const void*>(gather_finish_kernel), (int)smem);
+                if (ea != cudaSuccess) return ea;
                 gather_finish_kernel<<<dim3(kGFParts, (unsigned)H), kFinThreads, smem, st>>>(
                     scores, T, rs, k, K, state, ccount, done + H, cand, T, a.keep, cache_cap, jpt);
             } else {
                 const int64_t rchunks = (rs + kCols - 1) / kCols;
                 const dim3 ggrid((unsigned)std::max<int64_t>(1, (rchunks + kGatherJ - 1) / kGatherJ), (unsigned)H);
                 gather_kernel<<<ggrid, kThreads, 0, st>>>(scores, T, rs, state, ccount, cand, T, vec);
-                static size_t attr = 0;
-                if (smem > attr) {                       // static + dynamic may exceed the 48 KB default
-                    cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                    attr = smem;
-                }
+                // static + dynamic may exceed the 48 KB default
+                cudaError_t ea = ensure_kernel_attrs(reinterpret_cast<const void*>(finish_kernel), (int)smem);
+                if (ea != cudaSuccess) return ea;
                 finish_kernel<<<(unsigned)H, kFinThreads, smem, st>>>(T, rs, k, K, state, ccount, cand, T, a.keep,
                                                                       cache_cap);
             }

@@ -137,7 +137,15 @@ __device__ __forceinline__ void staged_loop(uint64_t nchunks, SrcFn src, BodyFn 
         const int s = (int)(k % kStages);
         const uint32_t parity = (uint32_t)((k / kStages) & 1u);
         const bool ok = __syncthreads_and(mbar_wait(&bars[s], parity));
-        if (!ok) return;                           // recorded in g_kvq_wait_timeouts
+        if (!ok) {                                 // recorded in g_kvq_wait_timeouts
+            // every copy issued must land before the CTA exits: thread 0 waits
+            // (bounded) for this stage and each later one it has issued
+            if (threadIdx.x == 0)
+                for (uint64_t j = k; j < k + kStages && first + j * step < nchunks; ++j)
+                    mbar_wait(&bars[j % kStages], (uint32_t)((j / kStages) & 1u));
+            __syncthreads();
+            return;
+        }
         body(c, smem + s * kStageBytes);
         __syncthreads();                           // the stage is free again
         if (threadIdx.x == 0) {
@@ -1220,8 +1228,8 @@ int meta_kind(const QSpec& q) {
 }
 
 template <typename K>
-void ensure_smem(K kernel) {
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedSmem);
+bool ensure_smem(K kernel, int bytes = kStagedSmem) {
+    return ensure_kernel_attrs(reinterpret_cast<const void*>(kernel), bytes) == cudaSuccess;
 }
 
 unsigned staged_grid(int sms, uint64_t nchunks) {
@@ -1244,11 +1252,7 @@ bool staged_c_ok(const QSpec& q) {
 template <int BITS, bool ASYM, int G, int SDT, int ZDT>
 void wq_t_launch(const QArgs& a, uint64_t nchunks, cudaStream_t st) {
     const unsigned grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(nchunks, (uint64_t)sm_count()));
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(wq_t_kernel<BITS, ASYM, G, SDT, ZDT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
-        attr = true;
-    }
+    if (!ensure_smem(wq_t_kernel<BITS, ASYM, G, SDT, ZDT>, kWSmem)) return;    // the error stays the last error
     wq_t_kernel<BITS, ASYM, G, SDT, ZDT><<<grid, kWThreads, kWSmem, st>>>(a);
 }
 
@@ -1263,7 +1267,7 @@ void sq_t_launch(const QArgs& a, cudaStream_t st) {
     default: break;
     }
     const unsigned grid = staged_grid(sm_count(), nchunks);
-    ensure_smem(sq_t_kernel<BITS, ASYM, 128, SDT, ZDT>);
+    if (!ensure_smem(sq_t_kernel<BITS, ASYM, 128, SDT, ZDT>)) return;
     sq_t_kernel<BITS, ASYM, 128, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a);
 }
 
@@ -1300,11 +1304,7 @@ bool wq_c_launch(const QArgs& a, cudaStream_t st) {
     if (!encode_rows_map(q, a.x, &map)) return false;
     const uint64_t nchunks = ((uint64_t)q.outer * q.T + kCRows - 1) / kCRows;
     const unsigned grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(nchunks, (uint64_t)sm_count()));
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(wq_c_kernel<BITS, ASYM, G, SDT, ZDT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCSmem);
-        attr = true;
-    }
+    if (!ensure_smem(wq_c_kernel<BITS, ASYM, G, SDT, ZDT>, kCSmem)) return true;    // the error stays the last error
     wq_c_kernel<BITS, ASYM, G, SDT, ZDT><<<grid, kCThreads, kCSmem, st>>>(a, map);
     return true;
 }
@@ -1326,9 +1326,9 @@ void sq_c_launch(const QArgs& a, cudaStream_t st) {
     const uint64_t nchunks = ((uint64_t)q.outer * q.T + rc - 1) / rc;
     const unsigned grid = staged_grid(sm_count(), nchunks);
     switch (q.g) {
-    case 32: ensure_smem(sq_c_kernel<BITS, ASYM, 32, SDT, ZDT>); sq_c_kernel<BITS, ASYM, 32, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a); break;
-    case 64: ensure_smem(sq_c_kernel<BITS, ASYM, 64, SDT, ZDT>); sq_c_kernel<BITS, ASYM, 64, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a); break;
-    default: ensure_smem(sq_c_kernel<BITS, ASYM, 128, SDT, ZDT>); sq_c_kernel<BITS, ASYM, 128, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a); break;
+    case 32: if (ensure_smem(sq_c_kernel<BITS, ASYM, 32, SDT, ZDT>)) sq_c_kernel<BITS, ASYM, 32, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a); break;
+    case 64: if (ensure_smem(sq_c_kernel<BITS, ASYM, 64, SDT, ZDT>)) sq_c_kernel<BITS, ASYM, 64, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a); break;
+    default: if (ensure_smem(sq_c_kernel<BITS, ASYM, 128, SDT, ZDT>)) sq_c_kernel<BITS, ASYM, 128, SDT, ZDT><<<grid, kThr, kStagedSmem, st>>>(a); break;
     }
 }
 
@@ -1470,11 +1470,7 @@ struct WdsL {
         static void go(const QArgs& a, const DsStats& ctx, cudaStream_t st) {
             using Sh = DtShape<B, G, STATS, S, Z>;
             auto kernel = wds_t_kernel<B, A, G, STATS, S, Z>;
-            static bool attr = false;
-            if (!attr) {
-                cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
-                attr = true;
-            }
+            if (!ensure_smem(kernel, Sh::kSmem)) return;        // the error stays the last error
             const uint64_t nchunks = (uint64_t)a.q.outer * a.q.ngroups * (G / Sh::CR);
             const unsigned grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(nchunks, (uint64_t)sm_count()));
             kernel<<<grid, Sh::kThreads, Sh::kSmem, st>>>(a, ctx.partials, ctx.done, ctx.out);
