@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from gpu_util import kb, kq_of, meta_np_dtype
+from gpu_util import Guarded, kb, kq_of, meta_np_dtype
 from kv_cache_quantization_kvq_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -54,12 +54,13 @@ def run(b, case, check_every=False):
     cB, sB, zB, _, _ = b.kvq_quantized_sizes(shape, b.BF16, b.QParams(*[getattr(kq, f) for f in (
         "bits", "mode", "qmin", "qmax", "axis", "group")], 0, kq.scale_dtype, kq.zero_dtype))
     dev = torch.device("cuda")
-    codes = torch.zeros(max(cB, 1), dtype=torch.uint8, device=dev)
-    scale = torch.zeros(max(sB, 1), dtype=torch.uint8, device=dev)
-    zero = torch.zeros(max(zB, 1), dtype=torch.uint8, device=dev)
-    resid = torch.zeros(outer * (R + block) * C, dtype=torch.bfloat16, device=dev)
+    g = Guarded()                      # canary bytes around every buffer the calls write
+    codes = g.alloc(max(cB, 1), fill=0)
+    scale = g.alloc(max(sB, 1), fill=0)
+    zero = g.alloc(max(zB, 1), fill=0)
+    resid = g.alloc(outer * (R + block) * C * 2, fill=0).view(torch.bfloat16)
     wB = b.kvq_append_workspace(shape, b.BF16, kq, block)
-    ws = torch.empty(max(wB, 1), dtype=torch.uint8, device=dev)
+    ws = g.alloc(max(wB, 1))
     Xd = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).cuda()
     tq, nres, t = 0, 0, 0
     while t < T:
@@ -67,6 +68,7 @@ def run(b, case, check_every=False):
         chunk = Xd[:, t:t + n].contiguous()
         tq, nres = b.kvq_append(chunk, n, b.BF16, shape, kq, block, codes, scale, zero, resid, tq, nres, ws, wB)
         t += n
+        g.check("kvq_append")
         if check_every:
             compare(b, X[:, :t], oq, tq, nres, codes, scale, zero, resid, R, block)
     compare(b, X, oq, tq, nres, codes, scale, zero, resid, R, block)

@@ -27,7 +27,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from gpu_util import kb, kq_of
+from gpu_util import Guarded, kb, kq_of
 from kv_cache_quantization_kvq_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -85,11 +85,13 @@ def run_case(b, shape, group, kq, vq, seed, kind="normal"):
 
     dk, dv = upload(qk), upload(qv)
     qd = torch.from_numpy(q).cuda()
-    out = torch.full((outer, group, C), float("nan"), dtype=torch.float32, device="cuda")
+    g = Guarded()                      # canary bytes around the output and the workspace
+    out = g.alloc(outer * group * C * 4).view(torch.float32).view(outer, group, C)
+    out.fill_(float("nan"))
     wB = b.kvq_attend_workspace(shape, group)
-    ws = torch.empty(max(wB, 1), dtype=torch.uint8, device="cuda")
+    ws = g.alloc(wB)
     b.kvq_attend_decode(qd, group, *dk, kq_of(b, kq), *dv, kq_of(b, vq), shape, out, ws, wB)
-    torch.cuda.synchronize()
+    g.check("kvq_attend_decode")
     got = out.cpu().numpy().astype(np.float64)
     tol = bound(q.astype(np.float64), K, V, splits=-(-T // 256))
     err = np.abs(got - want)

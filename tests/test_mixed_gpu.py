@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from gpu_util import kb
+from gpu_util import Guarded, kb
 from kv_cache_quantization_kvq_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -93,13 +93,15 @@ def run(b, shape, tags, kind="normal", seed=0, one_level=None):
     dev = torch.device("cuda")
     xd = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).cuda()
     td = torch.from_numpy(np.ascontiguousarray(tags, dtype=np.uint8)).cuda()
-    sbuf = torch.zeros(sB, dtype=torch.uint8, device=dev)
-    off = torch.zeros(oB // 8, dtype=torch.int64, device=dev)
-    t2 = torch.zeros(tB, dtype=torch.uint8, device=dev)
-    out = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    g = Guarded()                      # canary bytes around every written buffer
+    sbuf = g.alloc(sB)
+    off = g.alloc(oB).view(torch.int64)
+    t2 = g.alloc(tB)
+    out = g.alloc(outer * T * C * 2).view(torch.bfloat16).view(shape)
     b.kvq_mixed_quantize(xd, td, shape, sbuf, off, t2)
+    g.check("kvq_mixed_quantize")
     b.kvq_mixed_dequantize(sbuf, off, t2, shape, out)
-    torch.cuda.synchronize()
+    g.check("kvq_mixed_dequantize")
     streams, offs, t2w, deq = expected(X, tags) if one_level is None else expected_one_level(X, one_level)
     got_off = off.cpu().numpy().reshape(outer, T + 1)
     assert np.array_equal(got_off, offs), "record offsets differ"

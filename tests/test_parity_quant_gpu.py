@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from gpu_util import kb, kq_of, meta_np_dtype, to_device, to_host
+from gpu_util import Guarded, kb, kq_of, meta_np_dtype, to_device, to_host
 from kv_cache_quantization_kvq_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -48,16 +48,19 @@ def make_input(rng, shape, x_dtype, kind="normal"):
 
 def check_case(b, xin, x_dtype, oq, offset=0):
     """Run one case on both sides and compare.  offset > 0 shifts every
-    device buffer off 16-byte alignment to exercise the generic kernels."""
+    device buffer off 16-byte alignment to exercise the generic kernels.
+    Every buffer a call writes is a guarded window: canary bytes before and
+    after it must be unchanged after each call (no stray stores)."""
     import torch
     shape = xin.shape
     want = O.quantize(xin, x_dtype, oq)
     kq = kq_of(b, oq)
     cB, sB, zB, rB, wB = b.kvq_quantized_sizes(shape, x_dtype, kq)
     es = 2 if x_dtype == O.BF16 else 4
+    g = Guarded()
 
     def buf(n, off=offset):
-        return torch.zeros(n + 64, dtype=torch.uint8, device="cuda")[off:off + n] if n else None
+        return g.alloc(n, off)
 
     xraw = buf(xin.nbytes)
     if xin.nbytes:
@@ -65,6 +68,7 @@ def check_case(b, xin, x_dtype, oq, offset=0):
     codes, scale, zero, resid, ws = buf(cB), buf(sB), buf(zB), buf(rB), buf(wB, 0)
     b.kvq_quantize(xraw, x_dtype, shape, kq, codes, scale, zero, resid, ws, wB)
     torch.cuda.synchronize()
+    g.check("kvq_quantize")
     if cB:
         assert np.array_equal(to_host(codes), want.codes), "codes differ"
     if sB:
@@ -82,6 +86,7 @@ def check_case(b, xin, x_dtype, oq, offset=0):
         ob = buf(ref.nbytes)
         b.kvq_dequantize(codes, scale, zero, resid, shape, kq, ob, od)
         torch.cuda.synchronize()
+        g.check("kvq_dequantize")
         if ref.size:
             got = to_host(ob).view(ref.dtype).reshape(shape)
             assert np.array_equal(got, ref), f"dequantized values differ (out dtype {od})"
@@ -89,11 +94,12 @@ def check_case(b, xin, x_dtype, oq, offset=0):
     if xin.size:
         rmse, mx, mean = O.error_stats(xin, x_dtype, want, oq)
         sw = buf(wB, 0)
-        out = torch.zeros(3, dtype=torch.float64, device="cuda")
+        out = g.alloc(24).view(torch.float64)
         b.kvq_error_stats(xraw, x_dtype, codes, scale, zero, resid, shape, kq, out, sw, wB)
         torch.cuda.synchronize()
-        g = out.cpu().numpy()
-        for got, ref, name in ((g[0], rmse, "rmse"), (g[1], mx, "max"), (g[2], mean, "mean")):
+        g.check("kvq_error_stats")
+        gs = out.cpu().numpy()
+        for got, ref, name in ((gs[0], rmse, "rmse"), (gs[1], mx, "max"), (gs[2], mean, "mean")):
             assert got == pytest.approx(ref, rel=STATS_RTOL, abs=1e-30), name
 
 

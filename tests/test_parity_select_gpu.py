@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from gpu_util import kb, to_host
+from gpu_util import Guarded, kb, to_host
 from kv_cache_quantization_kvq_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -22,20 +22,30 @@ def b():
 
 
 def gpu_select(b, hist, budget, window, obs=None, offset=0, want_scores=True):
+    """One selection call; keep, scores and the workspace are guarded
+    windows whose surrounding canary bytes must survive the call."""
     import torch
     H, S, T = hist.shape
     raw = torch.zeros(hist.size + 16, dtype=torch.float32, device="cuda")
     h = raw[offset:offset + hist.size]
     h.copy_(torch.from_numpy(hist.ravel()).cuda())
-    keep = torch.full((H, min(budget, T)), -7, dtype=torch.int32, device="cuda")
-    scores = torch.zeros((H, T), dtype=torch.float32, device="cuda") if want_scores else None
+    g = Guarded()
+    K = min(budget, T)
+    keep_w = g.alloc(H * K * 4)
+    keep = keep_w.view(torch.int32).view(H, K) if keep_w is not None else torch.empty((H, K), dtype=torch.int32,
+                                                                                        device="cuda")
+    scores = None
+    if want_scores:
+        sw = g.alloc(H * T * 4)
+        scores = sw.view(torch.float32).view(H, T) if sw is not None else torch.empty((H, T), device="cuda")
     wB = b.kv_select_workspace(H, T)
-    ws = torch.empty(max(wB, 1), dtype=torch.uint8, device="cuda")
+    ws = g.alloc(wB)
     if obs is None:
         b.kv_h2o_select(h, H, S, T, budget, window, keep, scores, ws, wB)
     else:
         b.kv_snapkv_select(h, H, S, T, obs, budget, window, keep, scores, ws, wB)
     torch.cuda.synchronize()
+    g.check("selection")
     return to_host(keep), (to_host(scores) if want_scores else None)
 
 
@@ -86,6 +96,55 @@ def test_ties_signed_zeros_and_flat_rows(b):
         compare(b, hist, budget, window, obs=2)
 
 
+# Context lengths above 2^19 tokens take the other selection algorithm: a
+# level-1 histogram in the column sums, then three radix digits (12, 12 and 8
+# key bits) each by a histogram pass over the scores and a per-head digit
+# pick, per-chunk counts of keys above / equal to the k-th key, and an emit
+# pass that writes the heavy hitters (ties in index order) and the window.
+LONG_T = [524289, 600000]
+
+
+@pytest.mark.parametrize("T", LONG_T)
+def test_h2o_long_context_radix_path(b, T):
+    rng = np.random.default_rng(T)
+    hist = W.random_history(rng, 2, 4, T, planted=64, window=128)
+    for budget, window in ((1, 0), (2048, 128), (2048, 0), (T - 1, 128), (T - 1, 0), (T, 128), (5000, 5000)):
+        compare(b, hist, budget, window)
+
+
+@pytest.mark.parametrize("T", LONG_T)
+def test_snapkv_long_context_radix_path(b, T):
+    rng = np.random.default_rng(T + 3)
+    hist = W.random_history(rng, 2, 4, T, planted=64)
+    for budget, window in ((2048, 128), (1, 0)):
+        compare(b, hist, budget, window, obs=2)
+
+
+def test_long_context_flat_and_tied_heads(b):
+    """Every score of head 0 tied (flat rows): all three digit levels resolve
+    to one key and the tie pass keeps the lowest indices.  Head 1: a few
+    score values only, so the k-th key has many ties; head 2: signed zeros."""
+    rng = np.random.default_rng(7)
+    T = 600000
+    hist = np.empty((3, 2, T), np.float32)
+    hist[0] = 1.0 / T
+    hist[1] = rng.integers(0, 5, (2, T)) / 8.0
+    hist[2] = rng.choice(np.array([0.0, -0.0, 2.0 ** -20], np.float32), (2, T), p=[0.45, 0.45, 0.1])
+    for budget, window in ((2048, 128), (1, 0), (300000, 17), (T - 1, 1)):
+        compare(b, hist, budget, window)
+    compare(b, hist, 2048, 128, obs=1)
+
+
+def test_long_context_unaligned_history(b):
+    """T > 2^19 with a history that is not 16-byte aligned and T not a
+    multiple of 4: the scalar column-sum kernel of the radix path."""
+    rng = np.random.default_rng(11)
+    T = 524291
+    hist = W.random_history(rng, 2, 3, T, planted=16)
+    compare(b, hist, 2048, 128, offset=1)
+    compare(b, hist, 777, 0, offset=3, obs=2)
+
+
 def test_unaligned_history_scalar_path(b):
     rng = np.random.default_rng(2)
     hist = W.random_history(rng, 2, 5, 1000)
@@ -123,8 +182,11 @@ def test_compact(b, dtype, D):
     kv = torch.from_numpy(rng.standard_normal((H, T, D)).astype(np.float32) * 10).to(tdt).cuda()
     keep = np.sort(rng.choice(T, (H, K)), axis=1).astype(np.int32)
     keep[1] = rng.permutation(T)[:K]                            # order is the caller's
-    out = b.compact(kv, torch.from_numpy(keep).cuda())
-    torch.cuda.synchronize()
+    g = Guarded()
+    es = kv.element_size()
+    out = g.alloc(H * K * D * es).view(tdt).view(H, K, D)
+    b.compact(kv, torch.from_numpy(keep).cuda(), out=out)
+    g.check("kv_compact")
     host = to_host(kv)
     want = O.compact(host, keep)
     assert np.array_equal(to_host(out), want)
@@ -146,8 +208,12 @@ def test_compact_kv_pair(b, dtype, D):
     keep[1] = rng.permutation(T)[:K]
     keep[2, 5] = -1
     keep[2, 40] = T
-    ok, ov = b.compact_kv(k, v, torch.from_numpy(keep).cuda())
-    torch.cuda.synchronize()
+    g = Guarded()
+    nb = H * K * D * k.element_size()
+    ok = g.alloc(nb).view(tdt).view(H, K, D)
+    ov = g.alloc(nb, offset=16).view(tdt).view(H, K, D)
+    b.compact_kv(k, v, torch.from_numpy(keep).cuda(), out_k=ok, out_v=ov)
+    g.check("kv_compact_kv")
     for src, got in ((k, ok), (v, ov)):
         host = to_host(src)
         want = O.compact(host, np.clip(keep, 0, T - 1))

@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from gpu_util import kb
+from gpu_util import Guarded, kb
 from kv_cache_quantization_kvq_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -52,9 +52,14 @@ def run(b, shape, C, x_bf16, out_bf16, inverse, seed, inplace=False):
     sd = torch.from_numpy(s).cuda()
     ref = O.rotate(x64, s, inverse=inverse)
     od = b.BF16 if out_bf16 else b.F32
-    out = xd if inplace else None
+    g = Guarded()                      # canary bytes around the output
+    if inplace:
+        out = xd
+    else:
+        tdt = torch.bfloat16 if out_bf16 else torch.float32
+        out = g.alloc(x.size * (2 if out_bf16 else 4)).view(tdt).view(xd.shape)
     got = b.rotate(xd, sd, inverse=inverse, out=out, out_dtype=od)
-    torch.cuda.synchronize()
+    g.check("kvq_rotate")
     g = got.float().cpu().numpy().astype(np.float64)
     err = np.abs(g - ref)
     assert np.all(err <= tol(x64, ref, out_bf16)), f"max err {err.max():.3e}"
