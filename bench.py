@@ -44,6 +44,12 @@ FALLBACK_HBM_GBS = 6800.0
 KIVI = dict(batch=8, heads=8, T=8192, D=128, g=64, R=128)
 EVICT = dict(heads=32, steps=64, T=131072, D=128, budget=2048, window=128, obs=32)
 WORKLOAD_NAME = ("kivi_int4[b8,h8,T8192,d128,g64,R128] + h2o/snapkv[h32,S64,T131072,d128,B2048,W128,obs32]")
+# Rows timed beside the step (their own events and rooflines; not in `value`):
+# the largest quantize / dequantize workloads
+FULLMODEL = dict(layers=32, T=8192, heads=32, D=128)
+SWEEP = dict(batch=16, heads=8, T=32768, D=128)
+EXTRA_ROWS_NAME = ("rows: fullmodel_int8_per_channel[L32,T8192,H32,d128] K+V quantize/dequantize/error_stats; "
+                   "sweep_sym[b16,h8,T32768,d128] K+V int4 and int2 g64 per token quantize/dequantize")
 
 
 # ---------------------------------------------------------------- algorithmic bytes
@@ -407,27 +413,36 @@ def run_ours(args, rank, world, local_rank):
 
     # Timed region: K steps; before each, the L2 is flushed outside the step's
     # event interval; the step replays the graph (the KIVI, H2O and SnapKV
-    # rows as concurrent branches unless --serial-rows).
+    # rows as concurrent branches unless --serial-rows).  The K steps are
+    # repeated (each repeat bracketed by a barrier and a synchronize) until
+    # about --min-timed-seconds of steps have run; ms_per_step is the median
+    # repeat's mean step time, so the number rests on many clock samples.
     K = args.steps
-    ev_step = [mk() for _ in range(K)]
     launches = 0
+    rep_ms = []
     with ClockSampler(local_rank) as clk:
-        barrier()
         t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for i in range(K):
-                flush.zero_()
-                ev_step[i][0].record(stream)
-                if graph is not None:
-                    graph.replay()
-                    launches += per_step
-                else:
-                    for ph in phases:
-                        launches += getattr(st, ph)()
-                ev_step[i][1].record(stream)
-        barrier()
+        while True:
+            ev_step = [mk() for _ in range(K)]
+            barrier()
+            with torch.cuda.stream(stream):
+                for i in range(K):
+                    flush.zero_()
+                    ev_step[i][0].record(stream)
+                    if graph is not None:
+                        graph.replay()
+                        launches += per_step
+                    else:
+                        for ph in phases:
+                            launches += getattr(st, ph)()
+                    ev_step[i][1].record(stream)
+            barrier()
+            rep_ms.append(statistics.fmean(a.elapsed_time(z) for a, z in ev_step))
+            timed_s = sum(rep_ms) * K * 1e-3
+            if len(rep_ms) >= args.max_repeats or (len(rep_ms) >= 3 and timed_s >= args.min_timed_seconds):
+                break
         wall = time.perf_counter() - t0
-    step_ms = reduce_max_over_ranks(statistics.fmean(a.elapsed_time(z) for a, z in ev_step), world, dev)
+    step_ms = reduce_max_over_ranks(statistics.median(rep_ms), world, dev)
     total_bytes = sum(pbytes.values())
     value = whole_job_gbs(total_bytes, step_ms, world)
 
@@ -464,11 +479,23 @@ def run_ours(args, rank, world, local_rank):
                          "peak_kind": f"of {peak_kind}",
                          "bytes_per_launch": sel_B, "traffic": ncu_traffic()},
             "ms_per_step_rows_in_sequence": round(serial_ms, 5) if serial_ms else None,
-            "gpu_launches": launches,
-            "wait_timeouts": b.kvq_wait_timeouts(),    # bounded waits that gave up in this process: 0
+            "gpu_launches": launches,                    # all repeats of the timed region
+            "gpu_launches_per_step": launches // max(1, K * len(rep_ms)),
+            "timed_repeats": {"repeats": len(rep_ms), "steps_each": K,
+                              "ms_per_step_min": round(min(rep_ms), 5),
+                              "ms_per_step_median": round(statistics.median(rep_ms), 5),
+                              "ms_per_step_max": round(max(rep_ms), 5),
+                              "timed_s": round(sum(rep_ms) * K * 1e-3, 3)},
             "wall_s_timed_region": round(wall, 3),
             "clocks": clk.summary(),
         }
+        if args.only == "all" and not args.no_extra_rows:
+            # the largest quantize / dequantize workloads, each op its own row
+            rows, rclk = run_extra_rows(b, dev, stream, flush, peak, runs=max(5, min(args.steps, 50)))
+            result["phases"].update(rows)
+            result["config"]["workload"] = WORKLOAD_NAME + "; " + EXTRA_ROWS_NAME
+            result["clocks"] = {**result["clocks"], "extra_rows": rclk}
+        result["wait_timeouts"] = b.kvq_wait_timeouts()    # bounded waits that gave up in this process: 0
         if args.only != "all":
             result["config"]["only"] = args.only
         if args.evict_tokens is not None:
@@ -656,6 +683,94 @@ def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32,
     return out
 
 
+def fullmodel_bytes():
+    """Symmetric INT8 per channel over all T, fp32 scale, K and V together:
+    quantize reads x and writes codes + scales; dequantize the reverse; the
+    statistics read x, codes and scales."""
+    L, T, H, D = (FULLMODEL[k] for k in ("layers", "T", "heads", "D"))
+    x = 2 * L * T * H * D * 2
+    codes = 2 * L * T * H * D
+    scales = 2 * L * H * D * 4
+    return dict(quantize=x + codes + scales, dequantize=x + codes + scales, error_stats=x + codes + scales)
+
+
+def sweep_bytes(bits, g):
+    """Symmetric per token (groups of g channels), bf16 scale, K and V."""
+    n = 2 * SWEEP["batch"] * SWEEP["heads"] * SWEEP["T"] * SWEEP["D"]
+    q = n * 2 + n * bits // 8 + (n // g) * 2
+    return dict(quantize=q, dequantize=q)
+
+
+def run_extra_rows(b, dev, stream, flush, peak, runs=20):
+    """Full-model INT8 (quantize, dequantize, statistics) and the per-token
+    INT4 / INT2 g 64 sweep (quantize, dequantize), K and V inside one event
+    pair per op; median of `runs` with the L2 flushed before each.  Returns
+    the rows (with bytes and a roofline each) and the clock samples taken
+    while they ran."""
+    import torch
+    from kv_cache_quantization_kvq_gb300 import workloads as W
+    rows = {}
+
+    def med(fn):
+        ts = []
+        with torch.cuda.stream(stream):
+            fn()
+            for _ in range(runs):
+                flush.zero_()
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                z.record(stream)
+                ts.append((a, z))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(z) for a, z in ts)
+
+    def add(name, ms, nbytes):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "bytes": nbytes,
+                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                   "frac": round(gbs / peak, 4)}}
+
+    def qdq(tag, K, V, qp, nbytes, stats):
+        shape = tuple(K.shape)
+        qk, wk = b.alloc_quantized(shape, b.BF16, qp, dev)
+        qv, wv = b.alloc_quantized(shape, b.BF16, qp, dev)
+        ok, ov = torch.empty_like(K), torch.empty_like(V)
+        ek = torch.zeros(3, dtype=torch.float64, device=dev)
+        ev = torch.zeros(3, dtype=torch.float64, device=dev)
+
+        def quant():
+            b.quantize(K, qp, out=qk, workspace=wk, stream=stream)
+            b.quantize(V, qp, out=qv, workspace=wv, stream=stream)
+
+        def dequant():
+            b.dequantize(qk, out=ok, stream=stream)
+            b.dequantize(qv, out=ov, stream=stream)
+
+        def errs():
+            b.error_stats(K, qk, workspace=wk, stream=stream, out_dev=ek)
+            b.error_stats(V, qv, workspace=wv, stream=stream, out_dev=ev)
+
+        add(f"{tag}/quantize", med(quant), nbytes["quantize"])
+        add(f"{tag}/dequantize", med(dequant), nbytes["dequantize"])
+        if stats:
+            add(f"{tag}/error_stats", med(errs), nbytes["error_stats"])
+            assert torch.isfinite(ek).all() and torch.isfinite(ev).all()
+        del qk, qv, wk, wv, ok, ov
+
+    with ClockSampler(dev.index or 0) as clk:
+        K, V = W.fullmodel_kv(dev, seed=3, **FULLMODEL)
+        qdq("3_fullmodel_int8", K, V, b.QParams.sym(8, axis=b.ALONG_T, group=0), fullmodel_bytes(), True)
+        del K, V
+        K, V = W.sweep_kv(dev, seed=4, **SWEEP)
+        for bits in (4, 2):
+            qdq(f"4_sweep_int{bits}_g64", K, V, b.QParams.sym(bits, axis=b.ALONG_C, group=64, scale_dtype=b.BF16),
+                sweep_bytes(bits, 64), False)
+        del K, V
+        torch.cuda.empty_cache()
+    return rows, clk.summary()
+
+
 def run_e2e(b, st, stream, dev, args, total_bytes, world):
     """Same step through the C ABI with host buffers: pinned host -> device
     copies of every input, the step, device -> host copies of the results."""
@@ -825,6 +940,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-rows", action="store_true",
+                    help="skip the full-model INT8 and g/bit sweep rows timed beside the step")
+    ap.add_argument("--min-timed-seconds", type=float, default=1.0,
+                    help="repeat the K timed steps until about this much step time has run (at least 3 repeats)")
+    ap.add_argument("--max-repeats", type=int, default=400)
     ap.add_argument("--configs", action="store_true",
                     help="add the per-configuration table (tiny, KIVI INT4, full-model INT8, g/bit sweep)")
     ap.add_argument("--serial-rows", action="store_true",

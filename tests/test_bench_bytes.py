@@ -46,3 +46,17 @@ def test_eviction_bytes():
     assert eb["h2o_compact"] == eb["snapkv_compact"] == rows == 67_108_864
     assert eb["h2o_select"] + eb["h2o_compact"] == 1_141_112_832
     assert eb["snapkv_select"] + eb["snapkv_compact"] == 604_241_920
+
+
+def test_fullmodel_and_sweep_row_bytes():
+    """Full-model INT8 (32 layers x 8192 tokens x 4096 channels, K and V):
+    4,294,967,296 B of bf16 read, 2,147,483,648 B of codes and 262,144 fp32
+    scales (1,048,576 B) written -- 6,443,499,520 B per op.  Sweep (16 x 8
+    slices x 32768 tokens x 128 channels, K and V = 1,073,741,824 numbers):
+    2,147,483,648 B read; INT4 g 64 writes 536,870,912 B of codes and
+    33,554,432 B of bf16 scales, INT2 g 64 268,435,456 + 33,554,432 B."""
+    bn = _bench()
+    fm = bn.fullmodel_bytes()
+    assert fm["quantize"] == fm["dequantize"] == fm["error_stats"] == 6_443_499_520
+    assert bn.sweep_bytes(4, 64)["quantize"] == 2_147_483_648 + 570_425_344 == 2_717_908_992
+    assert bn.sweep_bytes(2, 64)["dequantize"] == 2_147_483_648 + 301_989_888
