@@ -852,6 +852,27 @@ SAMPLE_DESC = ("oracle (plain C, 1 thread) on 1 of 64 [batch*head] slices of the
                "workload (H2O + SnapKV select, compaction of K and V); GB/s = the slice's algorithmic bytes / time")
 
 
+def host_cpu():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        fields = {line.split(":", 1)[0].strip(): line.split(":", 1)[1].strip()
+                  for line in out.splitlines() if ":" in line}
+        name = " ".join(v for v in (fields.get("Vendor ID"), fields.get("Model name")) if v and v != "-")
+        if name:
+            return name
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
 def cpu_baseline(min_seconds=10.0):
     import oracle as O
     O.build()
@@ -865,7 +886,7 @@ def cpu_baseline(min_seconds=10.0):
         if el >= min_seconds:
             break
     return {"value": round(nbytes / el / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{SAMPLE_DESC}; {done} repetitions in {el:.1f} s"}
+            "host_cpu": host_cpu(), "sample": f"{SAMPLE_DESC}; {done} repetitions in {el:.1f} s"}
 
 
 def _oracle_worker(job):

@@ -354,11 +354,13 @@ KVQ_API kvq_status kvq_error_stats_noalloc(const void* x, kvq_dtype x_dtype, con
  * records itself in a device counter and the kernel leaves its loop, so its
  * outputs are undefined.  (The cluster kernels' barriers are hardware cluster
  * barriers that every CTA of the cluster reaches on every path, timeouts
- * included.)  This call synchronises
- * the current device (all streams), then writes to *count the number of such
- * waits since the library was loaded, over all kernels.  0 is the only value a
- * correct run produces.  Host pointer; KVQ_EINVAL if NULL, KVQ_ECUDA if the
- * synchronisation reports an error. */
+ * included.)  This call synchronises the current device (all streams), then
+ * writes to *count the number of such waits on the CURRENT DEVICE since the
+ * library was loaded there, over all kernels (each device keeps its own
+ * counters; call it once per device to cover several).  0 is the only value
+ * a correct run produces.  Host pointer; KVQ_EINVAL if NULL, KVQ_ECUDA if the
+ * synchronisation or the read of a counter reports an error (*count is then
+ * not written). */
 KVQ_API kvq_status kvq_wait_timeouts(uint64_t* count);
 
 /* Message describing the last non-OK status returned on this thread. */
