@@ -127,10 +127,15 @@ colsum_hist_kernel(const SelectArgs a, int64_t rs, float* scores, uint32_t* hist
     }
 }
 
-// Column sums for the candidate path: CTA (bx, h) walks chunks bx, bx+gx, ...
-// of head h, so its shared-memory histogram of candidate keys (top 12 bits)
-// is flushed once; the last CTA of the head to finish picks the level-1 bin
-// b1 holding the k-th largest key (state[h] = {b1, keys above b1}).
+// Column sums for the candidate path: the gx CTAs of head h split its columns
+// evenly, in 32-column (128-byte) groups, and CTA (bx, h) walks its own range
+// in steps of kCols columns.  Equal ranges make the CTAs finish together, and
+// contiguous ranges starting at unrelated offsets spread the concurrent
+// accesses over the memory channels (CTAs that strided through 4 KB chunks
+// whose offsets differ by powers of two measured up to 1.5x slower on some
+// GPUs).  Each CTA flushes its shared-memory histogram of candidate keys (top
+// 12 bits) once; the last CTA of the head to finish picks the level-1 bin b1
+// holding the k-th largest key (state[h] = {b1, keys above b1}).
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
 colsum_bin1_kernel(const SelectArgs a, int64_t rs, int64_t k, float* scores, uint32_t* hist1, uint32_t* done,
@@ -145,12 +150,14 @@ colsum_bin1_kernel(const SelectArgs a, int64_t rs, int64_t k, float* scores, uin
     const int64_t T = a.T;
     const int64_t nr = a.nrows;
     const float* base = a.hist + (h * a.steps + a.row0) * T;
-    const int64_t nchunks = (T + kCols - 1) / kCols;
-    for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
-        const int64_t col0 = chunk * kCols + threadIdx.x * 4;
+    const int64_t g32 = (T + 31) / 32;                          // 32-column groups of the head
+    const int64_t lo = (int64_t)blockIdx.x * g32 / gridDim.x * 32;
+    const int64_t hi = min(T, ((int64_t)blockIdx.x + 1) * g32 / gridDim.x * 32);
+    for (int64_t c0 = lo; c0 < hi; c0 += kCols) {
+        const int64_t col0 = c0 + threadIdx.x * 4;
         float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (VEC) {
-            if (col0 < T) {
+            if (col0 < hi) {
                 const float4* p = reinterpret_cast<const float4*>(base + col0);
                 const int64_t rstride = T / 4;
                 int64_t t = 0;
@@ -178,7 +185,7 @@ colsum_bin1_kernel(const SelectArgs a, int64_t rs, int64_t k, float* scores, uin
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int64_t col = col0 + j;
-                if (col < T)
+                if (col < hi)
                     for (int64_t t = 0; t < nr; ++t) s[j] = __fadd_rn(s[j], base[t * T + col]);
             }
         }
@@ -186,13 +193,16 @@ colsum_bin1_kernel(const SelectArgs a, int64_t rs, int64_t k, float* scores, uin
         for (int j = 0; j < 4; ++j) {
             if (a.divide) s[j] = __fdiv_rn(s[j], (float)nr);
             const int64_t col = col0 + j;
-            if (col < T) {
+            if (col < hi) {
                 if (!VEC) scores[h * T + col] = s[j];
                 if (want_bin && col < rs) atomicAdd(&sh[score_key(s[j]) >> 20], 1u);
             }
         }
-        if (VEC && col0 < T) *reinterpret_cast<float4*>(scores + h * T + col0) = make_float4(s[0], s[1], s[2], s[3]);
+        if (VEC && col0 < hi) *reinterpret_cast<float4*>(scores + h * T + col0) = make_float4(s[0], s[1], s[2], s[3]);
     }
+    // the selection kernel that follows may be scheduled from here on; it
+    // waits for this whole grid (and its memory) before reading anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!want_bin) return;
     __syncthreads();
     for (int i = threadIdx.x; i < kBins1; i += kThreads)
@@ -537,7 +547,69 @@ gather_kernel(const float* scores, int64_t T, int64_t rs, const uint32_t* state,
     }
 }
 
+// The bin, counted from the top of hist[0..nbins), where the running count
+// reaches r (1 <= r <= sum of hist), and r minus the count of the bins above
+// it.  Every one of the kFinThreads threads calls it and gets the result.
+__device__ __forceinline__ void rank_bin(const uint32_t* hist, int nbins, uint32_t r, uint32_t& bin, uint32_t& rem)
+{
+    __shared__ uint32_t s_res[2];
+    const int bpt = (nbins + kFinThreads - 1) / kFinThreads;      // 4 at most
+    const int top = nbins - 1 - (int)threadIdx.x * bpt;
+    uint32_t cnt[4] = {0u, 0u, 0u, 0u};
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (j < bpt && top - j >= 0) { cnt[j] = hist[top - j]; local += (int)cnt[j]; }
+    int total;
+    const int excl = block_excl_scan_n<kFinThreads>(local, total);
+    if ((uint32_t)excl < r && r <= (uint32_t)(excl + local)) {
+        uint32_t acc = (uint32_t)excl;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < bpt && acc + cnt[j] >= r) {
+                s_res[0] = (uint32_t)(top - j);
+                s_res[1] = r - acc;
+                break;
+            }
+            acc += cnt[j];
+        }
+    }
+    __syncthreads();
+    bin = s_res[0];
+    rem = s_res[1];
+    __syncthreads();
+}
+
+// Calls emit(position, index) for the set bits of bm[0..nwords) in index
+// order (positions 0, 1, ...).  Every one of the kFinThreads threads calls it.
+template <typename F>
+__device__ __forceinline__ void scan_bits(const uint32_t* bm, int nwords, F emit)
+{
+    const int wpt = (nwords + kFinThreads - 1) / kFinThreads;
+    const int w0 = (int)threadIdx.x * wpt;
+    int local = 0;
+    for (int j = 0; j < wpt; ++j)
+        if (w0 + j < nwords) local += __popc(bm[w0 + j]);
+    int total;
+    int pos = block_excl_scan_n<kFinThreads>(local, total);
+    for (int j = 0; j < wpt; ++j) {
+        if (w0 + j >= nwords) break;
+        uint32_t w = bm[w0 + j];
+        while (w) {
+            const int bit = __ffs(w) - 1;
+            w &= w - 1;
+            emit(pos, (w0 + j) * 32 + bit);
+            ++pos;
+        }
+    }
+}
+
 // The keep set of head h from its candidate list (kFinThreads threads).
+// Kept: every candidate above bin b1, plus the best `need` of bin b1 by (key
+// desc, index asc).  Radix levels 2 (12 bits) and 3 (8 bits) among the
+// members of bin b1 give the exact k-th key and how many of its ties to
+// keep; the ties are taken in index order; a scan of the kept bitmap writes
+// the indices ascending, then the recent window follows.
 __device__ __forceinline__ void finish_head(int64_t h, int64_t T, int64_t rs, int64_t k, int64_t K,
                                             const uint32_t* state, int64_t m, const uint2* ch, int32_t* keep,
                                             int64_t cache_cap)
@@ -546,193 +618,69 @@ __device__ __forceinline__ void finish_head(int64_t h, int64_t T, int64_t rs, in
     // copy of the head's candidates when there are at most cache_cap of them
     extern __shared__ uint32_t bitmap[];
     __shared__ uint32_t hist[kBins2];
-    __shared__ int wsum[32];
-    __shared__ uint32_t s_val[2];
     const uint32_t b1 = __ldcg(&state[h * 4 + 0]);
     const int64_t above = (int64_t)__ldcg(&state[h * 4 + 1]);
     const int nwords = (int)((T + 31) / 32);
-    if (m <= cache_cap) {                 // three passes below read the candidates: keep them on chip
+    uint32_t* ties = bitmap + nwords;
+    if (m <= cache_cap) {                 // the passes below read the candidates: keep them on chip
         uint2* cs = reinterpret_cast<uint2*>(bitmap + 2 * nwords);
         for (int64_t i = threadIdx.x; i < m; i += kFinThreads) cs[i] = __ldcg(&ch[i]);
-        __syncthreads();
         ch = cs;
     }
-    int32_t* kh = keep + h * K;
-
-    // Kept: every candidate above bin b1, plus the best `need` of bin b1 by
-    // (key desc, index asc).  When bin b1 holds at most kFinThreads keys they
-    // are ranked directly (each against all others); otherwise radix levels
-    // 2 and 3 find the exact k-th key and the ties are taken in index order.
-    const uint32_t need = (uint32_t)(k - above);
-    __shared__ uint2 binc[kFinThreads];
-    __shared__ int s_nb;
-    if (threadIdx.x == 0) s_nb = 0;
-    for (int i = threadIdx.x; i < nwords; i += kFinThreads) bitmap[i] = 0;
+    for (int i = threadIdx.x; i < nwords; i += kFinThreads) { bitmap[i] = 0; ties[i] = 0; }
+    for (int b = threadIdx.x; b < kBins2; b += kFinThreads) hist[b] = 0;
     __syncthreads();
+    const uint32_t need = (uint32_t)(k - above);            // >= 1: bin b1 holds the k-th key
+
+    // level 2 among the members of bin b1
     for (int64_t i = threadIdx.x; i < m; i += kFinThreads) {
-        const uint2 c = ch[i];
-        const uint32_t bin = c.x >> 20;
-        if (bin > b1) {
-            atomicOr(&bitmap[c.y >> 5], 1u << (c.y & 31));
-        } else if (bin == b1) {
-            const int slot = atomicAdd(&s_nb, 1);
-            if (slot < kFinThreads) binc[slot] = c;
-        }
+        const uint32_t key = ch[i].x;
+        if ((key >> 20) == b1) atomicAdd(&hist[(key >> 8) & 0xFFFu], 1u);
     }
     __syncthreads();
-    const int nb = s_nb;
-    if (nb <= kFinThreads) {
-        if ((int)threadIdx.x < nb) {
-            const uint2 me = binc[threadIdx.x];
-            uint32_t rank = 0;
-            for (int j2 = 0; j2 < nb; ++j2) {
-                const uint2 o = binc[j2];
-                rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
-            }
-            if (rank < need) atomicOr(&bitmap[me.y >> 5], 1u << (me.y & 31));
-        }
-        __syncthreads();
+    uint32_t b2, rem2;
+    rank_bin(hist, kBins2, need, b2, rem2);
+    const uint32_t pre = (b1 << 12) | b2;
+    const uint32_t in_b2 = hist[b2];
+    // kept: keys > kth, and tneed of the nties keys equal to kth (lowest indices)
+    uint32_t kth, tneed, nties;
+    __syncthreads();                                          // every thread has read hist[b2]
+    if (in_b2 == rem2 && pre != 0u) {
+        // the whole sub-bin is kept: the boundary lies just below it
+        kth = (pre << 8) - 1u;
+        tneed = nties = 0u;
     } else {
-    // radix levels 2 and 3 among the candidates of bin b1
-    uint32_t prefix = b1, rem = need;
-    for (int level = 2; level <= 3; ++level) {
-        const int nbins = level == 2 ? kBins2 : kBins3;
-        for (int b = threadIdx.x; b < nbins; b += kFinThreads) hist[b] = 0;
+        // level 3 among the keys with that 24-bit prefix
+        for (int b = threadIdx.x; b < kBins3; b += kFinThreads) hist[b] = 0;
         __syncthreads();
         for (int64_t i = threadIdx.x; i < m; i += kFinThreads) {
             const uint32_t key = ch[i].x;
-            if (level == 2) { if ((key >> 20) == prefix) atomicAdd(&hist[(key >> 8) & 0xFFFu], 1u); }
-            else if ((key >> 8) == prefix) atomicAdd(&hist[key & 0xFFu], 1u);
+            if ((key >> 8) == pre) atomicAdd(&hist[key & 0xFFu], 1u);
         }
         __syncthreads();
-        const int bpt = (nbins + kFinThreads - 1) / kFinThreads;
-        const int top = nbins - 1 - (int)threadIdx.x * bpt;
-        int local = 0;
-        for (int j = 0; j < bpt; ++j)
-            if (top - j >= 0) local += (int)hist[top - j];
-        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-        int x = local;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) wsum[w] = x;
-        __syncthreads();
-        if (w == 0) {
-            int y = wsum[lane];
-            for (int o = 1; o < 32; o <<= 1) {
-                const int z = __shfl_up_sync(0xFFFFFFFFu, y, o);
-                if (lane >= o) y += z;
-            }
-            wsum[lane] = y;
-        }
-        __syncthreads();
-        const int incl = x + (w > 0 ? wsum[w - 1] : 0);
-        const int excl = incl - local;
-        if (excl < (int)rem && (int)rem <= incl) {
-            int acc = excl;
-            for (int j = 0; j < bpt; ++j) {
-                const int b = top - j;
-                if (b < 0) break;
-                if (acc + (int)hist[b] >= (int)rem) {
-                    s_val[0] = (prefix << (level == 2 ? 12 : 8)) | (uint32_t)b;
-                    s_val[1] = rem - (uint32_t)acc;
-                    break;
-                }
-                acc += (int)hist[b];
-            }
-        }
-        __syncthreads();
-        prefix = s_val[0];
-        rem = s_val[1];
-        __syncthreads();
+        uint32_t b3;
+        rank_bin(hist, kBins3, rem2, b3, tneed);
+        kth = (pre << 8) | b3;                                // the exact k-th key
+        nties = hist[b3];
     }
-    const uint32_t kth = prefix;
-    const uint32_t tneed = rem;
-    // keys of bin b1 above T* are kept; ties of T* by index
-    uint32_t* ties = bitmap + nwords;                    // second bitmap for the ties
-    for (int i = threadIdx.x; i < nwords; i += kFinThreads) ties[i] = 0;
-    __syncthreads();
+    const bool all_ties = tneed == nties;                    // every tie is kept: no index pass
+
     for (int64_t i = threadIdx.x; i < m; i += kFinThreads) {
         const uint2 c = ch[i];
-        if ((c.x >> 20) != b1) continue;
-        if (c.x > kth) atomicOr(&bitmap[c.y >> 5], 1u << (c.y & 31));
+        if (c.x > kth || (all_ties && c.x == kth)) atomicOr(&bitmap[c.y >> 5], 1u << (c.y & 31));
         else if (c.x == kth) atomicOr(&ties[c.y >> 5], 1u << (c.y & 31));
     }
     __syncthreads();
-    {
-        const int wpt = (nwords + kFinThreads - 1) / kFinThreads;
-        const int w0 = (int)threadIdx.x * wpt;
-        int local = 0;
-        for (int j = 0; j < wpt; ++j)
-            if (w0 + j < nwords) local += __popc(ties[w0 + j]);
-        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-        int x = local;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) wsum[w] = x;
-        __syncthreads();
-        if (w == 0) {
-            int y = wsum[lane];
-            for (int o = 1; o < 32; o <<= 1) {
-                const int z = __shfl_up_sync(0xFFFFFFFFu, y, o);
-                if (lane >= o) y += z;
-            }
-            wsum[lane] = y;
-        }
-        __syncthreads();
-        int before = x - local + (w > 0 ? wsum[w - 1] : 0);
-        for (int j = 0; j < wpt; ++j) {
-            if (w0 + j >= nwords) break;
-            uint32_t tw = ties[w0 + j];
-            while (tw) {
-                const int bit = __ffs(tw) - 1;
-                tw &= tw - 1;
-                if ((uint32_t)before < tneed) bitmap[w0 + j] |= 1u << bit;
-                ++before;
-            }
-        }
+    if (!all_ties) {
+        scan_bits(ties, nwords, [&](int p, int idx) {
+            if ((uint32_t)p < tneed) atomicOr(&bitmap[idx >> 5], 1u << (idx & 31));
+        });
         __syncthreads();
     }
-    }
-    // scan the kept bitmap in index order and write the indices ascending
-    {
-        const int wpt = (nwords + kFinThreads - 1) / kFinThreads;
-        const int w0 = (int)threadIdx.x * wpt;
-        int local = 0;
-        for (int j = 0; j < wpt; ++j)
-            if (w0 + j < nwords) local += __popc(bitmap[w0 + j]);
-        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-        int x = local;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) wsum[w] = x;
-        __syncthreads();
-        if (w == 0) {
-            int y = wsum[lane];
-            for (int o = 1; o < 32; o <<= 1) {
-                const int z = __shfl_up_sync(0xFFFFFFFFu, y, o);
-                if (lane >= o) y += z;
-            }
-            wsum[lane] = y;
-        }
-        __syncthreads();
-        int pos = x - local + (w > 0 ? wsum[w - 1] : 0);
-        for (int j = 0; j < wpt; ++j) {
-            if (w0 + j >= nwords) break;
-            uint32_t bw = bitmap[w0 + j];
-            while (bw) {
-                const int bit = __ffs(bw) - 1;
-                bw &= bw - 1;
-                if (pos < k) kh[pos] = (int32_t)((w0 + j) * 32 + bit);
-                ++pos;
-            }
-        }
-    }
+    int32_t* kh = keep + h * K;
+    scan_bits(bitmap, nwords, [&](int p, int idx) {
+        if (p < k) kh[p] = idx;
+    });
     // the recent window follows the heavy hitters
     for (int64_t i = rs + threadIdx.x; i < T; i += kFinThreads) kh[k + (i - rs)] = (int32_t)i;
 }
@@ -760,8 +708,11 @@ gather_finish_kernel(const float* scores, int64_t T, int64_t rs, int64_t k, int6
 {
     __shared__ uint32_t s_base;
     __shared__ bool s_last;
+    // launched as a programmatic dependent of the column sums: nothing is read
+    // before that grid has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t h = blockIdx.y;
-    const uint32_t thr = __ldg(&state[h * 4 + 0]) << 20;        // lowest key of bin b1
+    const uint32_t thr = __ldcg(&state[h * 4 + 0]) << 20;       // lowest key of bin b1
     const float* sh = scores + (uint64_t)h * (uint64_t)T;
     const uint32_t rs32 = (uint32_t)rs;
     const uint32_t span = (uint32_t)jpt * 4u * kFinThreads;       // columns per part
@@ -869,8 +820,21 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st)
             if (jpt <= kGFMaxJ && vec && T >= 4) {
                 cudaError_t ea = ensure_kernel_attrs(reinterpret_cast<const void*>(gather_finish_kernel), (int)smem);
                 if (ea != cudaSuccess) return ea;
-                gather_finish_kernel<<<dim3(kGFParts, (unsigned)H), kFinThreads, smem, st>>>(
-                    scores, T, rs, k, K, state, ccount, done + H, cand, T, a.keep, cache_cap, jpt);
+                // programmatic dependent launch: its launch overlaps the column sums' tail
+                cudaLaunchConfig_t cfg = {};
+                cudaLaunchAttribute at[1];
+                at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                at[0].val.programmaticStreamSerializationAllowed = 1;
+                cfg.gridDim = dim3(kGFParts, (unsigned)H);
+                cfg.blockDim = dim3(kFinThreads);
+                cfg.dynamicSmemBytes = smem;
+                cfg.stream = st;
+                cfg.attrs = at;
+                cfg.numAttrs = 1;
+                cudaError_t el = cudaLaunchKernelEx(&cfg, gather_finish_kernel, (const float*)scores, T, rs, k, K,
+                                                    (const uint32_t*)state, ccount, done + H, cand, (int64_t)T, a.keep,
+                                                    cache_cap, jpt);
+                if (el != cudaSuccess) return el;
             } else {
                 const int64_t rchunks = (rs + kCols - 1) / kCols;
                 const dim3 ggrid((unsigned)std::max<int64_t>(1, (rchunks + kGatherJ - 1) / kGatherJ), (unsigned)H);
