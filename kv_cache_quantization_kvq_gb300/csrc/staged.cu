@@ -1080,6 +1080,16 @@ wds_t_kernel(const QArgs a, Partial* partials, unsigned int* done, kvq_err* out_
             bulk_g2s(st + L::offS, static_cast<const unsigned char*>(a.scale) + (uint64_t)grp * L::kSB, L::kSB, &full[s]);
             if (L::kZB)
                 bulk_g2s(st + L::offZ, static_cast<const unsigned char*>(a.zero) + (uint64_t)grp * L::kZB, L::kZB, &full[s]);
+            if (!STATS) {
+                // dequantize: the codes one ring-length ahead into L2 (measured
+                // faster; the statistics' larger tiles measured slower with it)
+                const uint32_t cq = c + (uint32_t)S * step;
+                if (cq < nchunks && cq > c) {
+                    uint32_t po, pgrp, prow0, pn;
+                    geom(cq, po, pgrp, prow0, pn);
+                    if (pn) bulk_prefetch_l2(codes + ((uint64_t)po * Tq32 + prow0) * L::kCodeRowB, pn * L::kCodeRowB);
+                }
+            }
         }
         for (uint32_t i = n > (uint32_t)S ? n - S : 0; i < n; ++i) mbar_wait(&full[i % S], (i / S) & 1u);
         return;
