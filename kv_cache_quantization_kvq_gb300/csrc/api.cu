@@ -191,9 +191,9 @@ int sm_count()
     return n;
 }
 
-cudaError_t ensure_kernel_attrs(const void* fn, int smem_bytes, bool nonportable_cluster)
+cudaError_t ensure_kernel_attrs(const void* fn, int smem_bytes, bool nonportable_cluster, bool max_carveout)
 {
-    struct Entry { const void* fn; int dev; int smem; bool npc; };
+    struct Entry { const void* fn; int dev; int smem; bool npc, carve; };
     static std::mutex mu;
     static std::vector<Entry> table;
     int dev = 0;
@@ -203,17 +203,21 @@ cudaError_t ensure_kernel_attrs(const void* fn, int smem_bytes, bool nonportable
     Entry* hit = nullptr;
     for (Entry& t : table)
         if (t.fn == fn && t.dev == dev) { hit = &t; break; }
-    if (hit && hit->smem >= smem_bytes && (hit->npc || !nonportable_cluster)) return cudaSuccess;
+    if (hit && hit->smem >= smem_bytes && (hit->npc || !nonportable_cluster) && (hit->carve || !max_carveout))
+        return cudaSuccess;
     const int want = hit ? std::max(hit->smem, smem_bytes) : smem_bytes;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
     if (e == cudaSuccess && nonportable_cluster)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess && max_carveout)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;      // also the thread's last error: the launch path reports it
     if (hit) {
         hit->smem = want;
         hit->npc = hit->npc || nonportable_cluster;
+        hit->carve = hit->carve || max_carveout;
     } else {
-        table.push_back(Entry{fn, dev, want, nonportable_cluster});
+        table.push_back(Entry{fn, dev, want, nonportable_cluster, max_carveout});
     }
     return cudaSuccess;
 }

@@ -133,11 +133,13 @@ cudaError_t launch_compact_pair(const void* k, const void* v, size_t elem, int64
 int sm_count();
 
 // Raise kernel fn's dynamic shared-memory limit to smem_bytes (and allow
-// non-portable cluster sizes when asked) on the current device: once per
-// (device, kernel), under a lock, so several host threads and several
+// non-portable cluster sizes, or ask for the largest shared-memory carve-out
+// so that several CTAs fit on an SM, when asked) on the current device: once
+// per (device, kernel), under a lock, so several host threads and several
 // devices in one process are safe.  Returns the error of a failed
 // cudaFuncSetAttribute, which also stays the thread's last error.
-cudaError_t ensure_kernel_attrs(const void* fn, int smem_bytes, bool nonportable_cluster = false);
+cudaError_t ensure_kernel_attrs(const void* fn, int smem_bytes, bool nonportable_cluster = false,
+                                bool max_carveout = false);
 
 // set the thread's kvq_last_error() message (printf-style)
 void set_last_error(const char* fmt, ...);

@@ -7,8 +7,10 @@ the comparison isolates the attention kernel.  The oracle computes in binary64
 logit_t = q.k_t / sqrt(d), y = sum_t softmax(logits)_t v_t, the cache rows as
 s * (q - zp) in full precision); the kernel computes in float32.
 
-Tolerance, derived from the kernel's float32 arithmetic (u = 2^-24,
-gamma_n = n u / (1 - n u), worst case, no probabilistic model):
+Tolerance, derived from the kernel's arithmetic (u = 2^-24,
+gamma_n = n u / (1 - n u), worst case, no probabilistic model).
+
+CUDA-core path (8-bit codes), float32 throughout:
  - a base-2 logit is a sum of C products q_c * k_tc, each rounded once when
    the K scale is folded into q, accumulated as two FMA chains of C/2 terms,
    added, and scaled by the rounded log2(e)/sqrt(C):
@@ -19,6 +21,19 @@ gamma_n = n u / (1 - n u), worst case, no probabilistic model):
  - y = sum_t p_t v_t / sum_t p_t moves by at most twice that times
    max_t |v_tc|, plus the accumulation of at most 64 tokens per warp, the
    merges and the division: gamma_{72 + splits} * max_t |v_tc|.
+
+Tensor-core path (2- and 4-bit codes, mma.sync bf16 x bf16 -> float32):
+ - each float32 factor x = q_c * s_c (logits) or p_t * s_t (values) enters as
+   bf16 hi + lo with |x - hi - lo| <= 2^-16 |x| (two 8-bit significands);
+   the integer factors (code - zero point) are exact in bf16;
+ - the products are exact in float32 and a logit accumulates 8 mma steps
+   (16 products each) and a warp's value at most 4; taking 2 ulp per step,
+   8 * 2^-22 = 2^-19 relative to the sum of magnitudes;
+ - so |d l_t| <= 2^-15 * log2(e)/sqrt(C) * sum_c |q_c k_tc| (2^-16 + 2^-19 +
+   a few u, doubled), and the value sums gain at most 2^-15 * max_t |v_tc|
+   on top of the float32 terms above.
+Tiles with residual tokens (and groups whose zero points bf16 cannot hold)
+take the float32 path, so the larger bound covers every token.
 """
 import math
 import zlib
@@ -53,16 +68,24 @@ def upload(qt):
             (qt.codes, qt.scale, qt.zero, qt.resid)]
 
 
-def bound(q, K, V, splits):
-    """Per-output tolerance (see the module docstring). q [O, G, C], K / V [O, T, C]."""
+def bound(q, K, V, splits, tc=False):
+    """Per-output tolerance (see the module docstring). q [O, G, C], K / V [O, T, C];
+    tc: the tensor-core path (2- and 4-bit codes)."""
     C = q.shape[-1]
     S = np.einsum("ojc,otc->ojt", np.abs(q), np.abs(K))                 # sum_c |q_c k_tc|
-    dl = gamma(C / 2 + 4) * math.log2(math.e) / math.sqrt(C) * S.max(-1)
+    coef = 2.0 ** -15 if tc else gamma(C / 2 + 4)
+    dl = coef * math.log2(math.e) / math.sqrt(C) * S.max(-1)
     logit = np.einsum("ojc,otc->ojt", q, K) * math.log2(math.e) / math.sqrt(C)
     spread = logit.max(-1) - logit.min(-1)
     e_p = math.log(2) * (2 * dl + U * spread) + 16 * U
     vmax = np.abs(V).max(axis=1)[:, None, :]                              # [O, 1, C]
-    return (2 * e_p[..., None] + gamma(72 + splits)) * vmax
+    return (2 * e_p[..., None] + gamma(72 + splits) + (2.0 ** -15 if tc else 0.0)) * vmax
+
+
+def uses_tensor_cores(kq, group):
+    """The dispatcher's rule: 2- and 4-bit caches read by 8 query heads per KV
+    slice take the tensor-core kernel."""
+    return kq.bits in (2, 4) and group == 8
 
 
 def run_case(b, shape, group, kq, vq, seed, kind="normal"):
@@ -72,10 +95,13 @@ def run_case(b, shape, group, kq, vq, seed, kind="normal"):
     if kind == "normal":
         xk = W.random_kv(rng, shape)
         xv = W.random_kv(rng, shape)
-    else:                                   # "peaked": a few dominant keys
+    elif kind == "peaked":                  # a few dominant keys
         xk = (rng.standard_normal(shape) * 0.2).astype(np.float32)
         xk[:, rng.integers(0, T, 3), :] *= 40.0
         xv = rng.standard_normal(shape).astype(np.float32)
+    else:                                   # "offset": values near +100, zero points far below 0
+        xk = (W.random_kv(rng, shape) + 100.0).astype(np.float32)
+        xv = (W.random_kv(rng, shape) + 100.0).astype(np.float32)
     xk, xv = W.to_bf16_bits(xk), W.to_bf16_bits(xv)
     q = rng.standard_normal((outer, group, C)).astype(np.float32)
     qk, qv = O.quantize(xk, O.BF16, kq), O.quantize(xv, O.BF16, vq)
@@ -93,7 +119,7 @@ def run_case(b, shape, group, kq, vq, seed, kind="normal"):
     b.kvq_attend_decode(qd, group, *dk, kq_of(b, kq), *dv, kq_of(b, vq), shape, out, ws, wB)
     g.check("kvq_attend_decode")
     got = out.cpu().numpy().astype(np.float64)
-    tol = bound(q.astype(np.float64), K, V, splits=-(-T // 256))
+    tol = bound(q.astype(np.float64), K, V, splits=-(-T // 256), tc=uses_tensor_cores(kq, group))
     err = np.abs(got - want)
     assert np.all(np.isfinite(got))
     assert np.all(err <= tol), f"max err {err.max():.3e}, worst err/tol {(err / tol).max():.3f}"
@@ -119,6 +145,17 @@ CASES = [
     ((3, 1), 8, O.QParams.sym(4, axis=O.ALONG_T, group=32), O.QParams.sym(4, axis=O.ALONG_C, group=32)),
     ((1, 4100), 4, O.QParams.asym(4, -8, 7, axis=O.ALONG_T, group=96, residual=3, zero_dtype=O.F32),
      O.QParams.asym(4, 0, 15, axis=O.ALONG_C, group=64, residual=3, zero_dtype=O.F32)),
+    # 8 query heads: the tensor-core kernel (2- and 4-bit), every V group size,
+    # symmetric (two's complement) and signed asymmetric codes, a tile that
+    # straddles the residual window, T a multiple of 16 and not
+    ((2, 300), 8, O.QParams.sym(2, axis=O.ALONG_T, group=0, residual=5, scale_dtype=O.BF16),
+     O.QParams.sym(2, axis=O.ALONG_C, group=32, residual=5, scale_dtype=O.BF16)),
+    ((2, 700), 8, O.QParams.sym(4, axis=O.ALONG_T, group=32, residual=64),
+     O.QParams.sym(4, axis=O.ALONG_C, group=128, residual=64)),
+    ((1, 4100), 8, O.QParams.asym(4, -8, 7, axis=O.ALONG_T, group=96, residual=3, zero_dtype=O.F32),
+     O.QParams.asym(4, 0, 15, axis=O.ALONG_C, group=64, residual=3, zero_dtype=O.F32)),
+    ((2, 1024), 8, O.QParams.asym(2, 0, 3, axis=O.ALONG_T, group=64, residual=0, scale_dtype=O.BF16, zero_dtype=O.BF16),
+     O.QParams.asym(2, 0, 3, axis=O.ALONG_C, group=64, residual=0, scale_dtype=O.BF16, zero_dtype=O.BF16)),
 ]
 
 
@@ -131,6 +168,16 @@ def test_attend_matches_oracle(b, case):
 def test_attend_peaked_scores(b):
     """A few keys 40x larger: nearly one-hot weights, large logit spread."""
     run_case(b, (2, 2000, 128), 2, KIVI_K, KIVI_V, 7, kind="peaked")
+    run_case(b, (2, 2000, 128), 8, KIVI_K, KIVI_V, 8, kind="peaked")
+
+
+def test_attend_large_offsets_take_the_exact_path(b):
+    """Caches whose values sit near +100: the asymmetric zero points fall far
+    below 0, outside the small integers bf16 holds exactly, and the tiles
+    concerned take the float32 path of the 8-head kernel; 1 head for the
+    CUDA-core kernel."""
+    for group in (8, 1):
+        run_case(b, (2, 600, 128), group, KIVI_K, KIVI_V, 9 + group, kind="offset")
 
 
 def test_attend_kivi_workload_full_size(b):
@@ -176,7 +223,7 @@ def test_attend_output_shift_within_value_error_bound(b):
     b.kvq_attend_decode(qd, 1, *dk, kq_of(b, KIVI_K), *dv, kq_of(b, KIVI_V), shape, out, ws, wB)
     torch.cuda.synchronize()
     got = out.cpu().numpy().astype(np.float64)
-    tol = bound(q.astype(np.float64), K, Vh, splits=-(-shape[1] // 256))
+    tol = bound(q.astype(np.float64), K, Vh, splits=-(-shape[1] // 256), tc=uses_tensor_cores(KIVI_K, 1))
     dy = np.linalg.norm(got - y_exact_v, axis=-1)                       # [O, 1]
     dv_max = np.linalg.norm(Vh - V, axis=-1).max(axis=1)[:, None]       # [O, 1]
     assert np.all(np.isfinite(got))
