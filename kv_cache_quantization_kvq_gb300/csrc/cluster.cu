@@ -11,9 +11,13 @@
 // A unit is (outer slice, group along T, block of 64 channels).  One
 // thread-block cluster of NC CTAs takes a unit, so the group is read from HBM
 // exactly once:
-//  1. CTA r of the cluster loads rows [r*sl, (r+1)*sl) of the group (sl =
-//     ceil(group length / NC) <= 512 rows, or <= 1024 where clusters of 16
-//     cannot be resident) into its shared memory with 3-D TMA boxes of 256
+//  1. CTA r of the cluster takes rows [r*sl, (r+1)*sl) of the group (sl =
+//     ceil(group length / NC)).  Groups of up to 2048 tokens: sl <= 512 rows,
+//     all in shared memory (or <= 1024 where clusters of 16 cannot be
+//     resident), three CTAs per SM.  Longer groups: sl <= 1024 rows, the first
+//     512 in shared memory and the rest in registers (16 words of 16 bytes per
+//     thread, loaded with plain coalesced loads), two CTAs per SM and at most
+//     8 CTAs per cluster.  Shared-memory rows arrive by 3-D TMA boxes of 256
 //     rows x 64 channels, each completing on its own mbarrier (rows past the
 //     quantized tokens are zero-filled, not read);
 //  2. it folds the per-channel abs-max (or min and max) of its rows as bf16
@@ -23,14 +27,16 @@
 //     constants of the 64 channels and (cluster rank 0) stores the scales and
 //     zero points;
 //  4. every thread then quantizes its rows straight from shared memory and
-//     stores the codes.
+//     registers and stores the codes.
 // A second cluster barrier, arrived at after step 3 and waited on at exit,
 // keeps each CTA resident until its peers have read its partials.  With 64 KB
 // slices three CTAs share an SM, so while one cluster exchanges or quantizes
-// another is loading.  (Persistent clusters walking the units through a ring
-// of slices measured slower: fewer clusters are resident, and the adjacent
-// channel blocks read at the same time -- 128 bytes of every 8 KB row per
-// unit -- then span less of each row.)
+// another is loading.  For 8192-token groups the register rows halve the
+// cluster (8 CTAs instead of 16), which measured 0.81x the time; for groups
+// of 1024 to 2048 tokens the three-CTA form measured faster.  (Persistent
+// clusters walking the units through a ring of slices measured slower: fewer
+// clusters are resident, and the adjacent channel blocks read at the same
+// time -- 128 bytes of every 8 KB row per unit -- then span less of each row.)
 #include <algorithm>
 #include <mutex>
 
@@ -57,6 +63,9 @@ constexpr int kLMaxBoxes = 4;                    // at most 1024 rows per CTA
 constexpr uint32_t kLMaxCluster = 16;
 constexpr uint32_t kLSmemCap = kLMaxBoxes * kLBoxB + 128;   // dynamic shared memory (+ alignment slack)
 constexpr int64_t kLMaxGroup = 8192;             // 16 CTAs x 512 rows, or 8 x 1024
+constexpr int kLRegWords = 16;                   // 16-byte register words per thread: 512 rows per CTA
+constexpr uint32_t kLRegSmemRows = 512;          // rows in shared memory beside them
+constexpr int64_t kLRegMinGroup = 2048;          // longer groups take the register variant
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -84,9 +93,22 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-template <int BITS, bool ASYM>
-__global__ void __launch_bounds__(kLThreads, 3)
-wq_l_kernel(const QArgs a, const __grid_constant__ CUtensorMap tmap, uint32_t ncb, uint32_t nc)
+// One 16-byte global load that bypasses L1 (the rows are read once).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// NR = 0: every row of the CTA's slice is held in shared memory (three CTAs
+// per SM).  NR > 0: the first `smax` rows are held in shared memory and up to
+// kLRPP * NR more in registers, NR 16-byte words per thread loaded straight
+// from global memory (two CTAs per SM, so a thread has 128 registers).
+template <int BITS, bool ASYM, int NR>
+__global__ void __launch_bounds__(kLThreads, NR ? 2 : 3)
+wq_l_kernel(const QArgs a, const __grid_constant__ CUtensorMap tmap, uint32_t ncb, uint32_t nc, uint32_t smax)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // [rows][64] bf16, 128 B per row; TMA boxes land on 128-byte boundaries
@@ -108,7 +130,8 @@ wq_l_kernel(const QArgs a, const __grid_constant__ CUtensorMap tmap, uint32_t nc
     const uint32_t sl = (glen + nc - 1) / nc;
     const uint32_t r0 = min(rank * sl, glen);
     const uint32_t nrows = min(sl, glen - r0);
-    const uint32_t nbox = (nrows + kLBoxRows - 1) / kLBoxRows;
+    const uint32_t nsm = NR ? min(nrows, smax) : nrows;       // rows held in shared memory
+    const uint32_t nbox = (nsm + kLBoxRows - 1) / kLBoxRows;
     const int64_t t0 = gstart + r0;                            // first token of this CTA's rows
 
     if (tid == 0) {
@@ -123,25 +146,43 @@ wq_l_kernel(const QArgs a, const __grid_constant__ CUtensorMap tmap, uint32_t nc
 
     // ---- 2. per-thread fold over rows rr, rr + kLRPP, ... of 8 channels (c8)
     const int c8 = tid % kLTPR, rr = tid / kLTPR;
+    // rows nsm + rr + kLRPP * i held in registers, all loads in flight at once
+    uint4 rg[NR ? NR : 1];
+    if constexpr (NR > 0) {
+        const unsigned char* src = static_cast<const unsigned char*>(a.x) +
+                                   (((uint64_t)o * q.T + (uint64_t)(t0 + nsm)) * q.C + (uint64_t)cb * kLCB + c8 * 8) * 2;
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            const uint32_t r = nsm + rr + kLRPP * i;
+            rg[i] = r < nrows ? ld_stream16(src + (uint64_t)(rr + kLRPP * i) * q.C * 2) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
     uint32_t mn[4], mx[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p) { mn[p] = kBfPosInf2; mx[p] = ASYM ? kBfNegInf2 : 0u; }
+    auto fold = [&](const uint4& w) {
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            if (ASYM) { mn[p] = bmin2(mn[p], ws[p]); mx[p] = bmax2(mx[p], ws[p]); }
+            else mx[p] = bmax2(mx[p], babs2(ws[p]));
+        }
+    };
     bool ok = true;
     for (uint32_t b = 0; b < nbox; ++b) {
         ok = mbar_wait(&full[b], 0) && ok;                     // a timeout is recorded in g_kvq_wait_timeouts
 #pragma unroll
         for (int i = 0; i < kLBoxRows / kLRPP; ++i) {
             const uint32_t r = b * kLBoxRows + rr + kLRPP * i;
-            if (r < nrows) {
-                const uint4 w = *reinterpret_cast<const uint4*>(slice + r * kLRowB + c8 * 16);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    if (ASYM) { mn[p] = bmin2(mn[p], ws[p]); mx[p] = bmax2(mx[p], ws[p]); }
-                    else mx[p] = bmax2(mx[p], babs2(ws[p]));
-                }
+            if (r < nsm) {
+                fold(*reinterpret_cast<const uint4*>(slice + r * kLRowB + c8 * 16));
             }
         }
+    }
+    if constexpr (NR > 0) {
+#pragma unroll
+        for (int i = 0; i < NR; ++i)
+            if (nsm + rr + kLRPP * i < nrows) fold(rg[i]);
     }
     // lanes l, l^8, l^16, l^24 hold the same channels
 #pragma unroll
@@ -245,10 +286,21 @@ wq_l_kernel(const QArgs a, const __grid_constant__ CUtensorMap tmap, uint32_t nc
 #pragma unroll 4
                 for (int i = 0; i < kLBoxRows / kLRPP; ++i) {
                     const uint32_t r = b * kLBoxRows + rr + kLRPP * i;
-                    if (r < nrows) {
+                    if (r < nsm) {
                         const uint4 w = *reinterpret_cast<const uint4*>(slice + r * kLRowB + c8 * 16);
                         uint32_t cc[8];
                         codes_of(w, cc);
+                        store_codes<BITS>(cbase + (uint64_t)r * code_row_B, finish_word<BITS>(cc, q.is_signed));
+                    }
+                }
+            }
+            if constexpr (NR > 0) {
+#pragma unroll
+                for (int i = 0; i < NR; ++i) {
+                    const uint32_t r = nsm + rr + kLRPP * i;
+                    if (r < nrows) {
+                        uint32_t cc[8];
+                        codes_of(rg[i], cc);
                         store_codes<BITS>(cbase + (uint64_t)r * code_row_B, finish_word<BITS>(cc, q.is_signed));
                     }
                 }
@@ -318,24 +370,31 @@ int resident_clusters(K kernel, uint32_t nc, uint32_t smem) {
     return n;
 }
 
-template <int BITS, bool ASYM>
+template <int BITS, bool ASYM, int NR>
 bool wq_l_launch(const QArgs& a, cudaStream_t st) {
     const QSpec& q = a.q;
-    auto kernel = wq_l_kernel<BITS, ASYM>;
+    auto kernel = wq_l_kernel<BITS, ASYM, NR>;
     if (ensure_kernel_attrs(reinterpret_cast<const void*>(kernel), (int)kLSmemCap, true) != cudaSuccess) {
         cudaGetLastError();          // not handled here: the caller takes the two-pass path
         return false;
     }
-    // 512-row slices (64 KB: three CTAs per SM) and up to 16 CTAs per
-    // cluster; where 16-CTA clusters cannot be resident, 1024-row slices and
-    // up to 8 CTAs
     const int64_t glen = std::min(q.g, q.Tq);
-    uint32_t maxr = 512;
-    uint32_t nc = (uint32_t)((glen + maxr - 1) / maxr);
-    if (nc > 8 && resident_clusters(kernel, nc, maxr * kLRowB + 128) < 1) {
-        maxr = 1024;
-        nc = (uint32_t)((glen + maxr - 1) / maxr);
+    uint32_t maxr, smax;
+    if (NR > 0) {
+        // 512 rows in shared memory and up to 512 in registers per CTA, up
+        // to 8 CTAs per cluster
+        smax = kLRegSmemRows;
+        maxr = smax + kLRPP * NR;
+    } else {
+        // 512-row slices (64 KB: three CTAs per SM) and up to 16 CTAs per
+        // cluster; where 16-CTA clusters cannot be resident, 1024-row slices
+        // and up to 8 CTAs
+        maxr = 512;
+        if ((glen + maxr - 1) / maxr > 8 && resident_clusters(kernel, (uint32_t)((glen + maxr - 1) / maxr), maxr * kLRowB + 128) < 1)
+            maxr = 1024;
+        smax = maxr;
     }
+    const uint32_t nc = (uint32_t)((glen + maxr - 1) / maxr);
     const uint32_t ncb = (uint32_t)(q.C / kLCB);
     const int64_t units = q.outer * q.ngroups * (int64_t)ncb;
     if (units * nc >= (int64_t(1) << 31)) return false;
@@ -349,15 +408,22 @@ bool wq_l_launch(const QArgs& a, cudaStream_t st) {
     at[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(units * nc));
     cfg.blockDim = dim3(kLThreads);
-    cfg.dynamicSmemBytes = (size_t)maxr * kLRowB + 128;
+    cfg.dynamicSmemBytes = (size_t)smax * kLRowB + 128;
     cfg.stream = st;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, a, map, ncb, nc) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel, a, map, ncb, nc, smax) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
     return true;
+}
+
+// Groups longer than one slice hold part of each CTA's rows in registers.
+template <int BITS, bool ASYM>
+bool wq_l_dispatch(const QArgs& a, cudaStream_t st) {
+    if (std::min(a.q.g, a.q.Tq) > kLRegMinGroup) return wq_l_launch<BITS, ASYM, kLRegWords>(a, st);
+    return wq_l_launch<BITS, ASYM, 0>(a, st);
 }
 
 }  // namespace
@@ -374,9 +440,9 @@ bool cluster_quantize(const QArgs& a, cudaStream_t st)
     if (!cluster_quantize_supported(a.q)) return false;
     const bool asym = a.q.mode == KVQ_ASYM;
     switch (a.q.bits) {
-    case 8: return asym ? wq_l_launch<8, true>(a, st) : wq_l_launch<8, false>(a, st);
-    case 4: return asym ? wq_l_launch<4, true>(a, st) : wq_l_launch<4, false>(a, st);
-    default: return asym ? wq_l_launch<2, true>(a, st) : wq_l_launch<2, false>(a, st);
+    case 8: return asym ? wq_l_dispatch<8, true>(a, st) : wq_l_dispatch<8, false>(a, st);
+    case 4: return asym ? wq_l_dispatch<4, true>(a, st) : wq_l_dispatch<4, false>(a, st);
+    default: return asym ? wq_l_dispatch<2, true>(a, st) : wq_l_dispatch<2, false>(a, st);
     }
 }
 

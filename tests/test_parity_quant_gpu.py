@@ -184,11 +184,13 @@ def test_along_t_fast(b, case):
 
 # Long groups along T (one scale per channel over hundreds to thousands of
 # tokens), bf16 sources: the cluster kernel, where 1 to 16 CTAs share one
-# group of 64 channels (ceil(group / 512) CTAs, or ceil(group / 1024) where
-# clusters of 16 cannot be resident), one cluster per unit; groups beyond 8192
-# tokens take the two-pass path through the workspace.  Ragged last groups
-# (some CTAs of a cluster get no rows), residual windows, several channel
-# blocks, and many more units than resident clusters.
+# group of 64 channels, one cluster per unit.  Groups of up to 2048 tokens:
+# ceil(group / 512) CTAs with every row in shared memory; longer groups:
+# ceil(group / 1024) CTAs with 512 rows in shared memory and the rest in
+# registers (2049 tokens: 171 register rows per CTA, a ragged register tail).
+# Groups beyond 8192 tokens take the two-pass path through the workspace.
+# Ragged last groups (some CTAs of a cluster get no rows), residual windows,
+# several channel blocks, and many more units than resident clusters.
 LONG_T_CASES = [
     # bits, mode (qmin, qmax) or None, g, T, R, C, kind, outer
     (8, None, 0, 4100, 4, 128, "normal", 2),
@@ -201,6 +203,8 @@ LONG_T_CASES = [
     (8, (0, 255), 0, 9000, 0, 64, "normal", 2),
     (8, (0, 255), 600, 1300, 0, 2048, "normal", 8),
     (8, None, 0, 8192, 0, 512, "normal", 4),
+    (8, None, 2049, 4200, 5, 128, "wide", 3),
+    (4, (0, 15), 2100, 2101, 0, 64, "ties", 2),
 ]
 
 
