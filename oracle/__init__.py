@@ -75,9 +75,11 @@ def _load():
         lib.oracle_dequantize_f64.argtypes = [vp, vp, vp, vp, P, i32, vp]
         lib.oracle_attend.argtypes = [vp, i64, vp, vp, i64, i64, i64, vp]
         lib.oracle_rotate.argtypes = [vp, i64, i64, vp, i32, vp]
+        lib.oracle_rotate_fwht32.argtypes = [vp, i32, i64, i64, vp, i32, vp, i32]
         for f in ("oracle_sizes", "oracle_token_compression_ratio", "oracle_quantize",
                   "oracle_dequantize", "oracle_error_stats", "oracle_h2o_select",
-                  "oracle_snapkv_select", "oracle_compact", "oracle_dequantize_f64", "oracle_attend", "oracle_rotate"):
+                  "oracle_snapkv_select", "oracle_compact", "oracle_dequantize_f64", "oracle_attend", "oracle_rotate",
+                  "oracle_rotate_fwht32"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -256,6 +258,22 @@ def rotate(x: np.ndarray, signs: np.ndarray, inverse: bool = False) -> np.ndarra
     out = np.zeros_like(x)
     _check(_load().oracle_rotate(_ptr(x), x.size // C if C else 0, C, _ptr(signs), int(inverse), _ptr(out)),
            "rotate")
+    return out
+
+
+def rotate_fwht32(x: np.ndarray, x_dtype: int, signs: np.ndarray, inverse: bool = False,
+                  out_dtype: int = F32) -> np.ndarray:
+    """The rotation as the binary32 fast Walsh-Hadamard transform (stages of
+    channel bit 1, 2, 4, ... in that order, then the multiply by the binary32
+    nearest 1/sqrt(C)).  x: float32 values (F32) or bf16 bit patterns (BF16,
+    uint16); returns float32 values or bf16 bit patterns (out_dtype)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16 if x_dtype == BF16 else np.float32)
+    C = x.shape[-1]
+    signs = np.ascontiguousarray(signs, dtype=np.int8)
+    assert signs.shape == (C,)
+    out = np.zeros(x.shape, np.uint16 if out_dtype == BF16 else np.float32)
+    _check(_load().oracle_rotate_fwht32(_ptr(x), x_dtype, x.size // C if C else 0, C, _ptr(signs), int(inverse),
+                                        _ptr(out), out_dtype), "rotate_fwht32")
     return out
 
 

@@ -59,7 +59,11 @@
  *  - decode attention over a quantized cache takes its rows in full precision,
  *    s * (q - zp) in binary64 with the stored s and zp (a fused kernel rounds
  *    nothing to the cache dtype in between), the residual rows as stored, and
- *    computes the softmax attention itself in binary64.
+ *    computes the softmax attention itself in binary64;
+ *  - the rotation fused into quantize / dequantize rounds the rotated values
+ *    to bf16 (the dtype the unfused path stores them in) and forms them in
+ *    binary32 as the fast transform, stages of channel bit 1, 2, 4, ... in
+ *    that order; the stand-alone rotation is the binary64 matrix product.
  */
 #include <math.h>
 #include <stddef.h>
@@ -674,6 +678,49 @@ int oracle_rotate(const double* x, int64_t rows, int64_t C, const int8_t* signs,
     }
     free(H);
     free(u);
+    return OR_OK;
+}
+
+/* The same rotation evaluated in binary32 as the fast Walsh-Hadamard
+ * transform, for the rotation fused into quantize / dequantize: there the
+ * rotated values are rounded to bf16 and quantized, so the codes are decided
+ * on binary32 results and both sides must form them the same way.  The
+ * Sylvester recursion read as an algorithm: y = H_2n u is H_n applied to each
+ * half of u, then the halves combined as (top + bottom, top - bottom).
+ * Unrolled, for h = 1, 2, 4, ..., C/2 in that order, every channel pair
+ * (j, j + h) with bit h of j clear becomes (v_j + v_{j+h}, v_j - v_{j+h}),
+ * each one IEEE binary32 operation; then every value is multiplied by the
+ * binary32 nearest to 1/sqrt(C) (taken as 1/sqrt(C) in binary64, then rounded
+ * to binary32).  Forward flips the signed channels of x first, inverse flips
+ * the outputs.  x: [rows][C] in x_dtype (F32 or BF16); out: [rows][C] in
+ * out_dtype (F32, or BF16 rounded to nearest-even). */
+int oracle_rotate_fwht32(const void* x, int x_dtype, int64_t rows, int64_t C, const int8_t* signs, int inverse,
+                         void* out, int out_dtype)
+{
+    if (rows < 0 || C < 1 || (C & (C - 1)) != 0) return OR_EINVAL;
+    if ((x_dtype != OR_F32 && x_dtype != OR_BF16) || (out_dtype != OR_F32 && out_dtype != OR_BF16)) return OR_EINVAL;
+    float* v = (float*)malloc((size_t)C * sizeof(float));
+    if (!v) return OR_EINVAL;
+    const float scale = (float)(1.0 / sqrt((double)C));
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < C; ++c) {
+            const float xc = load_as_float(x, x_dtype, r * C + c);
+            v[c] = (!inverse && signs[c] < 0) ? -xc : xc;
+        }
+        for (int64_t h = 1; h < C; h *= 2)
+            for (int64_t j = 0; j < C; ++j)
+                if ((j & h) == 0) {
+                    const float a = v[j], b = v[j + h];
+                    v[j] = a + b;
+                    v[j + h] = a - b;
+                }
+        for (int64_t c = 0; c < C; ++c) {
+            float y = v[c] * scale;
+            if (inverse && signs[c] < 0) y = -y;
+            store_float(out, out_dtype, r * C + c, y);
+        }
+    }
+    free(v);
     return OR_OK;
 }
 

@@ -16,6 +16,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+from kv_cache_quantization_kvq_gb300 import workloads as W
 
 
 def load(golden_dir, name):
@@ -776,3 +777,80 @@ def test_rotate_equalises_variances():
     s = np.where(rng.random(C) < 0.5, -1, 1).astype(np.int8)
     cols = O.rotate(np.diag(np.sqrt(lam)), s)           # row c = rotation of sqrt(lam_c) e_c
     assert np.allclose((cols ** 2).sum(axis=0), lam.mean(), rtol=1e-12)
+
+
+# The same rotation in binary32 as the fast transform (the rotation fused into
+# quantize / dequantize decides codes on binary32 values rounded to bf16).
+
+U32 = 2.0 ** -24
+
+
+def fwht_bound(x64):
+    """|fast transform in binary32 - exact| <= gamma_{log2 C + 2} sum_c |x_c| / sqrt(C):
+    log2(C) additions of partial sums bounded by sum |x|, one multiply by the
+    rounded 1/sqrt(C) (gamma_n = n u / (1 - n u), u = 2^-24)."""
+    C = x64.shape[-1]
+    n = int(math.log2(C)) + 2
+    return (n * U32 / (1 - n * U32)) * np.abs(x64).sum(-1, keepdims=True) / math.sqrt(C)
+
+
+def test_rotate_fwht32_within_binary32_bound_of_matrix_product():
+    """Against the binary64 Sylvester matrix product, both directions, both
+    source dtypes (catches a dropped stage, a wrong sign or partner index)."""
+    rng = np.random.default_rng(60)
+    for C in (32, 64, 128, 256, 1024):
+        x = (rng.standard_normal((6, C)) * np.exp(rng.uniform(-4, 4, (6, 1)))).astype(np.float32)
+        s = np.where(rng.random(C) < 0.5, -1, 1).astype(np.int8)
+        for inverse in (False, True):
+            want = O.rotate(x.astype(np.float64), s, inverse=inverse)
+            got = O.rotate_fwht32(x, O.F32, s, inverse=inverse).astype(np.float64)
+            assert np.all(np.abs(got - want) <= fwht_bound(x.astype(np.float64))), (C, inverse)
+        xb = W.to_bf16_bits(x)
+        x64 = O.bf16_bits_to_f32(xb).astype(np.float64)
+        want = O.rotate(x64, s)
+        got = O.bf16_bits_to_f32(O.rotate_fwht32(xb, O.BF16, s, out_dtype=O.BF16)).astype(np.float64)
+        tol = 2.0 ** -8 * (np.abs(want) + fwht_bound(x64)) + fwht_bound(x64)   # plus the bf16 rounding
+        assert np.all(np.abs(got - want) <= tol), C
+
+
+def test_rotate_fwht32_exact_on_small_integers():
+    """Integer inputs with |x| <= 8: every partial sum is an integer below 2^24,
+    and 1/sqrt(C) is a power of two for C = 4^k, so the binary32 transform is
+    exact and equals the binary64 matrix product bit for bit."""
+    rng = np.random.default_rng(61)
+    for C in (64, 256, 1024):
+        x = rng.integers(-8, 9, (4, C)).astype(np.float32)
+        s = np.where(rng.random(C) < 0.5, -1, 1).astype(np.int8)
+        for inverse in (False, True):
+            got = O.rotate_fwht32(x, O.F32, s, inverse=inverse)
+            want = O.rotate(x.astype(np.float64), s, inverse=inverse)
+            assert np.array_equal(got.astype(np.float64), want), (C, inverse)
+
+
+def test_rotate_fwht32_stage_order_worked_example():
+    """Hand-derived: x = [1, 2^-24, -1, 2^-24], C = 4, no flips, scale 1/2.
+    Stage h = 1: 1 + 2^-24 ties to 1; 1 - 2^-24 exact; -1 + 2^-24 exact;
+    -1 - 2^-24 ties to -1, so v = [1, 1 - 2^-24, -(1 - 2^-24), -1].
+    Stage h = 2: 1 - (1 - 2^-24) = 2^-24; (1 - 2^-24) - 1 = -2^-24;
+    1 + (1 - 2^-24) = 2 - 2^-24 ties to 2, twice.  Times 1/2:
+    [2^-25, -2^-25, 1, 1].  (Stage h = 2 first would give the exact
+    [2^-24, -2^-24, 1, 1], so this pins the stage order.)"""
+    x = np.array([[1.0, 2.0 ** -24, -1.0, 2.0 ** -24]], np.float32)
+    got = O.rotate_fwht32(x, O.F32, np.ones(4, np.int8))
+    assert np.array_equal(got, np.array([[2.0 ** -25, -2.0 ** -25, 1.0, 1.0]], np.float32))
+    exact = O.rotate(x.astype(np.float64), np.ones(4, np.int8))
+    assert np.array_equal(exact, np.array([[2.0 ** -24, -2.0 ** -24, 1.0, 1.0]]))
+
+
+def test_rotate_fwht32_round_trip_and_bf16_rounding():
+    """Inverse after forward returns x within twice the bound; a bf16 output
+    is the nearest-even bf16 of the binary32 output."""
+    rng = np.random.default_rng(62)
+    C = 128
+    x = rng.standard_normal((5, C)).astype(np.float32)
+    s = np.where(rng.random(C) < 0.5, -1, 1).astype(np.int8)
+    y = O.rotate_fwht32(x, O.F32, s)
+    back = O.rotate_fwht32(y, O.F32, s, inverse=True).astype(np.float64)
+    assert np.all(np.abs(back - x) <= 2 * fwht_bound(x.astype(np.float64)) + 1e-6 * np.abs(x))
+    yb = O.rotate_fwht32(x, O.F32, s, out_dtype=O.BF16)
+    assert np.array_equal(yb, W.to_bf16_bits(y))
