@@ -652,7 +652,17 @@ def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32,
                         -1, 1).to(torch.int8)
     rot = torch.empty_like(K)
     out["2_kivi_int4/K/rotate"] = entry(med(lambda: b.rotate(K, signs, out=rot, stream=stream)), 2 * K.numel() * 2)
-    del K, V, rot
+    # the rotation fused into the value cache's per-token quantize and dequantize
+    # (the KIVI value format): the same bytes as the plain quantize / dequantize
+    vqf = b.QParams.asym(4, 0, 15, axis=b.ALONG_C, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
+    qvf, _ = b.alloc_quantized(tuple(V.shape), b.BF16, vqf, dev)
+    fq_B, _ = quant_bytes(tuple(V.shape), 2, *(t.numel() for t in (qvf.codes, qvf.scale, qvf.zero, qvf.resid)))
+    vout = torch.empty_like(V)
+    out["2_kivi_int4/V/rotate_quantize"] = entry(med(lambda: b.rotate_quantize(V, signs, vqf, out=qvf, stream=stream)),
+                                                 fq_B)
+    out["2_kivi_int4/V/dequantize_rotate"] = entry(med(lambda: b.dequantize_rotate(qvf, signs, out=vout, stream=stream)),
+                                                   fq_B)
+    del K, V, rot, qvf, vout
     # 3: full model INT8, per channel over all tokens
     K, V = W.fullmodel_kv(dev, seed=3)
     qdq("3_fullmodel_int8", [("K", K), ("V", V)], b.QParams.sym(8, axis=b.ALONG_T, group=0))

@@ -257,6 +257,34 @@ KVQ_API kvq_status kvq_attend_decode(const float* q, int64_t group, const void* 
 KVQ_API kvq_status kvq_rotate(const void* x, kvq_dtype x_dtype, const kvq_shape* shape, const int8_t* signs,
                               int inverse, void* out, kvq_dtype out_dtype, void* stream);
 
+/* The rotation above fused into per-token quantization and dequantization
+ * (KV-COBRA notes, "关键设计" item 4: the rotation absorbed into the quantize
+ * path), one read and one write of the tensor each:
+ *  - kvq_rotate_quantize: y = the forward rotation of x rounded to bf16 (what
+ *    kvq_rotate writes with out_dtype BF16), quantized with p exactly as
+ *    kvq_quantize quantizes y: codes / scale / zero of the first Tq tokens,
+ *    and the last min(R, T) tokens of y (rotated) in resid.
+ *  - kvq_dequantize_rotate: x_hat of the buffers rounded to bf16 (what
+ *    kvq_dequantize writes with out_dtype BF16; resid rows as stored), then the
+ *    inverse rotation rounded to bf16 into out.
+ * Each equals the two separate calls bit for bit.  The y tensor and x_hat
+ * never go to memory.
+ *  - x / out: [outer, T, C] bf16 only; groups along C (per token) only, C in
+ *    {32, 64, 128, 256} and the group a power of two from 32 to C
+ *    (KVQ_EUNSUPPORTED otherwise; other formats: kvq_rotate, then
+ *    kvq_quantize).  Buffers are laid out as kvq_quantize lays them out.
+ *  - signs: device int8 [C], as for kvq_rotate.
+ *  - x / out, codes and resid 16-byte aligned; scale and zero aligned to their
+ *    element size.  No workspace.
+ *  - Errors: KVQ_EINVAL (NULL or misaligned buffers, a bad format),
+ *    KVQ_EUNSUPPORTED, KVQ_ECUDA; nothing is launched on an error. */
+KVQ_API kvq_status kvq_rotate_quantize(const void* x, kvq_dtype x_dtype, const kvq_shape* shape, const int8_t* signs,
+                                       const kvq_qparams* p, void* codes, void* scale, void* zero, void* resid,
+                                       void* stream);
+KVQ_API kvq_status kvq_dequantize_rotate(const void* codes, const void* scale, const void* zero, const void* resid,
+                                         const kvq_shape* shape, const kvq_qparams* p, const int8_t* signs,
+                                         void* out, kvq_dtype out_dtype, void* stream);
+
 /* Online (streaming) quantized cache: append tokens, quantize full blocks.
  * [KVC] §"带残差区的压缩预算，逐项加起来": the most recent tokens stay in bf16 and
  * the older ones are stored quantized in groups; with one token per decode step

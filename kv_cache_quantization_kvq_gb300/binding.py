@@ -69,6 +69,8 @@ def _load() -> ctypes.CDLL:
         "kvq_attend_workspace": [S, i64, psz],
         "kvq_attend_decode": [vp, i64, vp, vp, vp, vp, P, vp, vp, vp, vp, P, S, vp, vp, sz, vp],
         "kvq_rotate": [vp, i32, S, vp, i32, vp, i32, vp],
+        "kvq_rotate_quantize": [vp, i32, S, vp, P, vp, vp, vp, vp, vp],
+        "kvq_dequantize_rotate": [vp, vp, vp, vp, S, P, vp, vp, i32, vp],
         "kvq_append_workspace": [S, i32, P, i64, psz],
         "kvq_mixed_sizes": [S, psz, psz, psz],
         "kvq_mixed_quantize": [vp, vp, S, vp, vp, vp, vp],
@@ -95,7 +97,7 @@ EXPORTS = ("kvq_quantized_sizes", "kvq_quantize", "kvq_dequantize", "kvq_error_s
            "kvq_compression_ratio", "kvq_token_compression_ratio", "kv_select_workspace",
            "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kv_compact_kv", "kvq_last_error", "kvq_version",
            "kvq_error_stats_noalloc", "kvq_attend_workspace", "kvq_attend_decode", "kvq_rotate",
-           "kvq_append_workspace", "kvq_append", "kvq_mixed_sizes", "kvq_mixed_quantize", "kvq_mixed_dequantize",
+           "kvq_rotate_quantize", "kvq_dequantize_rotate", "kvq_append_workspace", "kvq_append", "kvq_mixed_sizes", "kvq_mixed_quantize", "kvq_mixed_dequantize",
            "kvq_wait_timeouts")
 
 # size of the library's fixed scratch array behind kvq_error_stats_noalloc
@@ -261,6 +263,18 @@ def kvq_rotate(x, x_dtype, shape, signs, inverse, out, out_dtype, stream=None):
     s = _shape(shape)
     _check(LIB.kvq_rotate(_ptr(x), x_dtype, ctypes.byref(s), _ptr(signs), int(bool(inverse)), _ptr(out), out_dtype,
                           _stream(stream)))
+
+
+def kvq_rotate_quantize(x, x_dtype, shape, signs, qp: QParams, codes, scale, zero, resid, stream=None):
+    s, p = _shape(shape), qp.c()
+    _check(LIB.kvq_rotate_quantize(_ptr(x), x_dtype, ctypes.byref(s), _ptr(signs), ctypes.byref(p), _ptr(codes),
+                                   _ptr(scale), _ptr(zero), _ptr(resid), _stream(stream)))
+
+
+def kvq_dequantize_rotate(codes, scale, zero, resid, shape, qp: QParams, signs, out, out_dtype, stream=None):
+    s, p = _shape(shape), qp.c()
+    _check(LIB.kvq_dequantize_rotate(_ptr(codes), _ptr(scale), _ptr(zero), _ptr(resid), ctypes.byref(s),
+                                     ctypes.byref(p), _ptr(signs), _ptr(out), out_dtype, _stream(stream)))
 
 
 def kvq_append_workspace(shape, x_dtype, qp: QParams, block: int) -> int:
@@ -434,6 +448,25 @@ def attend_decode(q, qk: Quantized, qv: Quantized, out=None, workspace=None, str
         workspace = _empty(kvq_attend_workspace(qk.shape, group), q.device)
     kvq_attend_decode(q, group, qk.codes, qk.scale, qk.zero, qk.resid, qk.qp, qv.codes, qv.scale, qv.zero,
                       qv.resid, qv.qp, qk.shape, out, workspace, workspace.numel(), stream)
+    return out
+
+
+def rotate_quantize(x, signs, qp: QParams, out: Optional[Quantized] = None, stream=None) -> Quantized:
+    """x: CUDA bf16 [..., T, C] -> the quantized rotated tensor (groups along
+    C); the residual window holds rotated rows."""
+    shape = (x.numel() // (x.shape[-1] * x.shape[-2]) if x.shape[-1] * x.shape[-2] else 0, x.shape[-2], x.shape[-1])
+    if out is None:
+        out, _ = alloc_quantized(shape, BF16, qp, x.device)
+    kvq_rotate_quantize(x, torch_dtype_code(x), shape, signs, qp, out.codes, out.scale, out.zero, out.resid, stream)
+    return out
+
+
+def dequantize_rotate(qt: Quantized, signs, out=None, stream=None):
+    """The inverse of rotate_quantize: x_hat rotated back, bf16."""
+    import torch
+    if out is None:
+        out = torch.empty(qt.shape, dtype=torch.bfloat16, device=qt.codes.device)
+    kvq_dequantize_rotate(qt.codes, qt.scale, qt.zero, qt.resid, qt.shape, qt.qp, signs, out, BF16, stream)
     return out
 
 

@@ -435,6 +435,59 @@ kvq_status kvq_rotate(const void* x, kvq_dtype x_dtype, const kvq_shape* shape, 
 
 namespace {
 
+// Validation shared by the two fused rotation calls: the format, the shapes
+// the fused kernels take, the buffers' presence and alignment.
+kvq_status rotq_checks(const kvq_shape* shape, kvq_dtype dt, const kvq_qparams* p, const void* x, const char* xname,
+                       const int8_t* signs, const void* codes, const void* scale, const void* zero, const void* resid,
+                       kvq::QSpec& q)
+{
+    kvq_status s = make_spec(shape, dt, p, q);
+    if (s != KVQ_OK) return s;
+    if (dt != KVQ_BF16) return fail(KVQ_EUNSUPPORTED, "the fused rotation takes bf16 tensors only");
+    if (q.outer * q.T == 0) return KVQ_OK;
+    if (!kvq::rotq_supported(q))
+        return fail(KVQ_EUNSUPPORTED,
+                    "the fused rotation needs groups along C, C in {32, 64, 128, 256} and a group of 32..C channels, "
+                    "a power of two (got C = %lld, group = %lld, axis %d)", (long long)q.C, (long long)q.g, q.axis);
+    const Sizes z = sizes_of(q);
+    const size_t xB = (size_t)(q.outer * q.T * q.C) * 2;
+    if ((s = need_ptr(x, xB, xname)) || (s = need_ptr(codes, z.codes, "codes")) ||
+        (s = need_ptr(scale, z.scale, "scale")) || (s = need_ptr(zero, z.zero, "zero")) ||
+        (s = need_ptr(resid, z.resid, "resid")) || (s = need_ptr(signs, 1, "signs")))
+        return s;
+    if (!aligned16(x) || !aligned16(codes) || (z.resid && !aligned16(resid)))
+        return fail(KVQ_EINVAL, "%s, codes and resid must be 16-byte aligned", xname);
+    if ((s = need_align(scale, dtype_bytes(q.scale_dt), "scale")) || (s = need_align(zero, dtype_bytes(q.zero_dt), "zero")))
+        return s;
+    return KVQ_OK;
+}
+
+}  // namespace
+
+kvq_status kvq_rotate_quantize(const void* x, kvq_dtype x_dtype, const kvq_shape* shape, const int8_t* signs,
+                               const kvq_qparams* p, void* codes, void* scale, void* zero, void* resid, void* stream)
+{
+    kvq::QSpec q;
+    kvq_status s = rotq_checks(shape, x_dtype, p, x, "x", signs, codes, scale, zero, resid, q);
+    if (s != KVQ_OK || q.outer * q.T == 0) return s;
+    kvq::QArgs a = {x, codes, scale, zero, resid, nullptr, nullptr, 0, q};
+    return cuda_status(kvq::launch_rotate_quantize(a, signs, (cudaStream_t)stream), "kvq_rotate_quantize launch");
+}
+
+kvq_status kvq_dequantize_rotate(const void* codes, const void* scale, const void* zero, const void* resid,
+                                 const kvq_shape* shape, const kvq_qparams* p, const int8_t* signs, void* out,
+                                 kvq_dtype out_dtype, void* stream)
+{
+    kvq::QSpec q;
+    kvq_status s = rotq_checks(shape, out_dtype, p, out, "out", signs, codes, scale, zero, resid, q);
+    if (s != KVQ_OK || q.outer * q.T == 0) return s;
+    kvq::QArgs a = {nullptr, const_cast<void*>(codes), const_cast<void*>(scale), const_cast<void*>(zero),
+                    const_cast<void*>(resid), out, nullptr, 0, q};
+    return cuda_status(kvq::launch_dequantize_rotate(a, signs, (cudaStream_t)stream), "kvq_dequantize_rotate launch");
+}
+
+namespace {
+
 // The store's format and the one flush of the streaming cache: the buffer
 // [outer, R + block, C] quantized with residual R, into workspace buffers.
 struct AppendPlan {

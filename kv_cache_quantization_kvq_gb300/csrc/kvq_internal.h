@@ -95,6 +95,12 @@ cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st);
 cudaError_t launch_rotate(const void* x, int x_dt, void* out, int out_dt, const int8_t* signs, uint64_t rows,
                           int64_t C, int inverse, cudaStream_t st);
 
+// ---- the rotation fused into per-token quantize / dequantize (rotq.cu): bf16,
+// groups along C, C in {32, 64, 128, 256}, g a power of two in [32, C]
+bool rotq_supported(const QSpec& q);
+cudaError_t launch_rotate_quantize(const QArgs& a, const int8_t* signs, cudaStream_t st);
+cudaError_t launch_dequantize_rotate(const QArgs& a, const int8_t* signs, cudaStream_t st);
+
 // ---- strided row copy (append.cu): rows x width bytes, pitches in bytes
 cudaError_t launch_copy2d(void* dst, uint64_t dpitch, const void* src, uint64_t spitch, uint64_t width,
                           uint64_t rows, cudaStream_t st);

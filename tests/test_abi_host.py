@@ -33,7 +33,7 @@ def declared_symbols():
 
 def test_library_exports_every_declared_symbol(kb):
     declared = declared_symbols()
-    assert len(declared) == 23
+    assert len(declared) == 25
     for name in declared:
         assert hasattr(kb.LIB, name), name
     assert declared == set(kb.EXPORTS)
@@ -258,6 +258,39 @@ def test_rotate_rejected_before_launch(kb):
             kb.kvq_rotate(x, xd, shape, signs, False, fake, od, 0)
         assert e.value.status == status, (shape, str(e.value))
     kb.kvq_rotate(None, kb.BF16, (0, 10, 128), None, False, None, kb.BF16, 0)   # empty: nothing to do
+
+
+def test_fused_rotation_rejected_before_launch(kb):
+    """kvq_rotate_quantize / kvq_dequantize_rotate: formats and shapes the
+    fused kernels do not take, missing or misaligned buffers."""
+    fake = 1 << 20  # never dereferenced: validation fails first
+    v64 = kb.QParams.asym(4, 0, 15, axis=kb.ALONG_C, group=64, residual=4, scale_dtype=kb.BF16, zero_dtype=kb.BF16)
+    cases = (
+        ((2, 10, 128), kb.F32, v64, fake, fake, kb.EUNSUPPORTED),                                   # fp32 tensor
+        ((2, 10, 128), kb.BF16, kb.QParams.sym(4, axis=kb.ALONG_T, group=64), fake, fake, kb.EUNSUPPORTED),  # along T
+        ((2, 10, 128), kb.BF16, kb.QParams.sym(4, axis=kb.ALONG_C, group=16), fake, fake, kb.EUNSUPPORTED),  # g < 32
+        ((2, 10, 128), kb.BF16, kb.QParams.sym(4, axis=kb.ALONG_C, group=96), fake, fake, kb.EUNSUPPORTED),  # g not 2^k
+        ((2, 10, 512), kb.BF16, v64, fake, fake, kb.EUNSUPPORTED),                                  # C > 256
+        ((2, 10, 48), kb.BF16, kb.QParams.sym(4, axis=kb.ALONG_C, group=0), fake, fake, kb.EUNSUPPORTED),  # C
+        ((2, 10, 128), kb.BF16, v64, None, fake, kb.EINVAL),                                        # no signs
+        ((2, 10, 128), kb.BF16, v64, fake, None, kb.EINVAL),                                        # no tensor
+        ((2, 10, 128), kb.BF16, v64, fake, fake + 8, kb.EINVAL),                                    # misaligned
+        ((2, 10, 128), kb.BF16, kb.QParams.sym(4, qmax=9, axis=kb.ALONG_C, group=64), fake, fake, kb.EINVAL),  # format
+    )
+    for shape, dt, qp, signs, x, status in cases:
+        with pytest.raises(kb.KvqError) as e:
+            kb.kvq_rotate_quantize(x, dt, shape, signs, qp, fake, fake, fake, fake, 0)
+        assert e.value.status == status, ("quantize", shape, str(e.value))
+        with pytest.raises(kb.KvqError) as e:
+            kb.kvq_dequantize_rotate(fake, fake, fake, fake, shape, qp, signs, x, dt, 0)
+        assert e.value.status == status, ("dequantize", shape, str(e.value))
+    # codes misaligned
+    with pytest.raises(kb.KvqError) as e:
+        kb.kvq_rotate_quantize(fake, kb.BF16, (2, 10, 128), fake, v64, fake + 4, fake, fake, fake, 0)
+    assert e.value.status == kb.EINVAL
+    # empty tensors: nothing to do
+    kb.kvq_rotate_quantize(None, kb.BF16, (0, 10, 128), None, v64, None, None, None, None, 0)
+    kb.kvq_dequantize_rotate(None, None, None, None, (3, 0, 128), v64, None, None, kb.BF16, 0)
 
 
 def test_append_rejected_before_launch(kb):
