@@ -604,31 +604,31 @@ def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32,
     if only_attend:
         return out
     # streaming append: 64 decode steps of one token into the KIVI key and value
-    # caches (block 64: each cache flushes one block of 64 tokens), microseconds per step
+    # caches of one layer (block 64: the 32nd step flushes one block of 64 tokens
+    # of each cache), one kvq_append_kv call per step, microseconds per step
     kq_s = b.QParams.asym(4, 0, 15, axis=b.ALONG_T, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
     vq_s = b.QParams.asym(4, 0, 15, axis=b.ALONG_C, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
     cap_shape = (K.shape[0], K.shape[1], K.shape[2])
-    state = {}
+    stores = {}
     for name, qp in (("K", kq_s), ("V", vq_s)):
         store_qp = b.QParams(qp.bits, qp.mode, qp.qmin, qp.qmax, qp.axis, qp.group, 0, qp.scale_dtype, qp.zero_dtype)
         cB, sB, zB, _, _ = b.kvq_quantized_sizes(cap_shape, b.BF16, store_qp)
-        wB = b.kvq_append_workspace(cap_shape, b.BF16, qp, 64)
-        state[name] = [qp, torch.empty(cB, dtype=torch.uint8, device=dev), torch.empty(sB, dtype=torch.uint8, device=dev),
-                       torch.empty(zB, dtype=torch.uint8, device=dev),
-                       torch.empty(K.shape[0] * (128 + 64) * K.shape[2], dtype=torch.bfloat16, device=dev),
-                       torch.empty(wB, dtype=torch.uint8, device=dev), wB]
-    steps = [K[:, i:i + 1].contiguous() for i in range(64)]
+        stores[name] = (torch.empty(cB, dtype=torch.uint8, device=dev), torch.empty(sB, dtype=torch.uint8, device=dev),
+                        torch.empty(zB, dtype=torch.uint8, device=dev),
+                        torch.empty(K.shape[0] * (128 + 64) * K.shape[2], dtype=torch.bfloat16, device=dev))
+    wB = b.kvq_append_kv_workspace(cap_shape, b.BF16, kq_s, vq_s, 64)
+    aws = torch.empty(wB, dtype=torch.uint8, device=dev)
+    app = b.KVAppender(cap_shape, b.BF16, kq_s, vq_s, 64, stores["K"], stores["V"], aws, stream=stream)
+    ksteps = [K[:, i:i + 1].contiguous() for i in range(64)]
+    vsteps = [V[:, i:i + 1].contiguous() for i in range(64)]
 
     def decode_steps():
-        counters = {"K": [0, 160], "V": [0, 160]}     # 160 of 192 buffered: the 32nd step flushes
-        for x1 in steps:
-            for name in ("K", "V"):
-                qp, cd, sc, zr, rs, ws, wB = state[name]
-                counters[name] = list(b.kvq_append(x1, 1, b.BF16, cap_shape, qp, 64, cd, sc, zr, rs, *counters[name],
-                                                   ws, wB, stream))
+        app.set_counters(0, 160)                        # 160 of 192 buffered: the 32nd step flushes
+        for k1, v1 in zip(ksteps, vsteps):
+            app.append(k1, v1, 1)
     ms = med(decode_steps)
     out["2_kivi_int4/append_KV_one_token_us"] = round(1e3 * ms / 64, 2)
-    del state, steps
+    del stores, aws, app, ksteps, vsteps
     # per-token mixed precision of the key cache, the four levels in equal shares
     # (seeded tags): quantize reads K and writes the records, dequantize the reverse
     shp = tuple(K.shape)

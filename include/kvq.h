@@ -310,14 +310,35 @@ KVQ_API kvq_status kvq_dequantize_rotate(const void* codes, const void* scale, c
  *  - Errors: KVQ_EINVAL (bad counters, a store too small for the flushes the
  *    call needs, NULL or misaligned buffers), KVQ_EWORKSPACE; nothing is
  *    launched and the counters are unchanged then.
- *  - Cost: one quantize and four small copies per flush; a long prompt is
- *    better quantized with kvq_quantize before appending starts. */
+ *  - Cost: one copy launch per call without a flush; one quantize and one
+ *    copy launch per flush; a long prompt is better quantized with
+ *    kvq_quantize before appending starts. */
 KVQ_API kvq_status kvq_append_workspace(const kvq_shape* shape, kvq_dtype x_dtype, const kvq_qparams* p,
                                         int64_t block, size_t* workspace_B);
 KVQ_API kvq_status kvq_append(const void* x_new, int64_t n, kvq_dtype x_dtype, const kvq_shape* shape,
                               const kvq_qparams* p, int64_t block, void* codes, void* scale, void* zero,
                               void* resid, int64_t* tq, int64_t* nres, void* workspace, size_t workspace_B,
                               void* stream);
+
+/* The key and the value cache of one layer appended together, in one call
+ * that shares the counters (*tq, *nres): exactly kvq_append on K, then on V,
+ * with the same n, block and counters, bit for bit.  Each decode step without a
+ * flush is one kernel launch (the new K and V rows copied together); a flush
+ * is one quantize per cache and one launch for both caches' codes, metadata
+ * and kept rows.
+ *  - k_params / v_params: the two formats (keys typically grouped along T,
+ *    values along C); their residual windows must be equal (KVQ_EINVAL).
+ *  - k_* / v_*: each cache's store and buffer, as for kvq_append.
+ *  - workspace: at least kvq_append_kv_workspace bytes (K's part, then V's).
+ *  - Errors as kvq_append; nothing is launched and the counters are unchanged
+ *    on an error. */
+KVQ_API kvq_status kvq_append_kv_workspace(const kvq_shape* shape, kvq_dtype x_dtype, const kvq_qparams* k_params,
+                                           const kvq_qparams* v_params, int64_t block, size_t* workspace_B);
+KVQ_API kvq_status kvq_append_kv(const void* k_new, const void* v_new, int64_t n, kvq_dtype x_dtype,
+                                 const kvq_shape* shape, const kvq_qparams* k_params, const kvq_qparams* v_params,
+                                 int64_t block, void* k_codes, void* k_scale, void* k_zero, void* k_resid,
+                                 void* v_codes, void* v_scale, void* v_zero, void* v_resid, int64_t* tq,
+                                 int64_t* nres, void* workspace, size_t workspace_B, void* stream);
 
 /* Per-token mixed precision.  "大模型KV缓存自适应量化实战" §2.1: every token
  * is stored at one of four levels, 2/4/8/16 bits; §3.1: per-token

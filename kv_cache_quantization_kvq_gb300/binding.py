@@ -78,6 +78,9 @@ def _load() -> ctypes.CDLL:
         "kvq_wait_timeouts": [ctypes.POINTER(ctypes.c_uint64)],
         "kvq_append": [vp, i64, i32, S, P, i64, vp, vp, vp, vp, ctypes.POINTER(i64), ctypes.POINTER(i64), vp, sz,
                        vp],
+        "kvq_append_kv_workspace": [S, i32, P, P, i64, psz],
+        "kvq_append_kv": [vp, vp, i64, i32, S, P, P, i64, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(i64),
+                          ctypes.POINTER(i64), vp, sz, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -97,7 +100,8 @@ EXPORTS = ("kvq_quantized_sizes", "kvq_quantize", "kvq_dequantize", "kvq_error_s
            "kvq_compression_ratio", "kvq_token_compression_ratio", "kv_select_workspace",
            "kv_h2o_select", "kv_snapkv_select", "kv_compact", "kv_compact_kv", "kvq_last_error", "kvq_version",
            "kvq_error_stats_noalloc", "kvq_attend_workspace", "kvq_attend_decode", "kvq_rotate",
-           "kvq_rotate_quantize", "kvq_dequantize_rotate", "kvq_append_workspace", "kvq_append", "kvq_mixed_sizes", "kvq_mixed_quantize", "kvq_mixed_dequantize",
+           "kvq_rotate_quantize", "kvq_dequantize_rotate", "kvq_append_kv_workspace", "kvq_append_kv",
+           "kvq_append_workspace", "kvq_append", "kvq_mixed_sizes", "kvq_mixed_quantize", "kvq_mixed_dequantize",
            "kvq_wait_timeouts")
 
 # size of the library's fixed scratch array behind kvq_error_stats_noalloc
@@ -292,6 +296,58 @@ def kvq_append(x_new, n, x_dtype, shape, qp: QParams, block, codes, scale, zero,
                           _ptr(scale), _ptr(zero), _ptr(resid), ctypes.byref(t), ctypes.byref(r), _ptr(workspace),
                           int(workspace_B), _stream(stream)))
     return t.value, r.value
+
+
+def kvq_append_kv_workspace(shape, x_dtype, kqp: QParams, vqp: QParams, block: int) -> int:
+    s, pk, pv, n = _shape(shape), kqp.c(), vqp.c(), ctypes.c_size_t()
+    _check(LIB.kvq_append_kv_workspace(ctypes.byref(s), x_dtype, ctypes.byref(pk), ctypes.byref(pv), int(block),
+                                       ctypes.byref(n)))
+    return n.value
+
+
+def kvq_append_kv(k_new, v_new, n, x_dtype, shape, kqp: QParams, vqp: QParams, block, k_bufs, v_bufs, tq, nres,
+                  workspace, workspace_B, stream=None):
+    """k_bufs / v_bufs: (codes, scale, zero, resid) of each cache.  Returns the
+    updated (tq, nres) counters."""
+    s, pk, pv = _shape(shape), kqp.c(), vqp.c()
+    t, r = ctypes.c_int64(int(tq)), ctypes.c_int64(int(nres))
+    _check(LIB.kvq_append_kv(_ptr(k_new), _ptr(v_new), int(n), x_dtype, ctypes.byref(s), ctypes.byref(pk),
+                             ctypes.byref(pv), int(block), *[_ptr(x) for x in k_bufs], *[_ptr(x) for x in v_bufs],
+                             ctypes.byref(t), ctypes.byref(r), _ptr(workspace), int(workspace_B), _stream(stream)))
+    return t.value, r.value
+
+
+class KVAppender:
+    """Streaming append of one layer's K and V caches, one kvq_append_kv call
+    per decode step.  The ctypes arguments that do not change between steps
+    (shape, formats, buffers, workspace, stream) are built once; tq / nres are
+    the shared counters."""
+
+    def __init__(self, shape, x_dtype, kqp: QParams, vqp: QParams, block, k_bufs, v_bufs, workspace, tq=0, nres=0,
+                 stream=None):
+        self._s, self._pk, self._pv = _shape(shape), kqp.c(), vqp.c()
+        self._t, self._r = ctypes.c_int64(int(tq)), ctypes.c_int64(int(nres))
+        self._head = (x_dtype, ctypes.byref(self._s), ctypes.byref(self._pk), ctypes.byref(self._pv), int(block))
+        self._tail = tuple(_ptr(x) for x in k_bufs) + tuple(_ptr(x) for x in v_bufs) + (
+            ctypes.byref(self._t), ctypes.byref(self._r), _ptr(workspace), int(workspace.numel()), _stream(stream))
+        self._fn = LIB.kvq_append_kv
+
+    @property
+    def tq(self) -> int:
+        return self._t.value
+
+    @property
+    def nres(self) -> int:
+        return self._r.value
+
+    def set_counters(self, tq: int, nres: int):
+        self._t.value, self._r.value = int(tq), int(nres)
+
+    def append(self, k_new, v_new, n: int):
+        """k_new, v_new: CUDA [outer, n, C] contiguous, the cache's dtype."""
+        st = self._fn(k_new.data_ptr(), v_new.data_ptr(), n, *self._head, *self._tail)
+        if st != OK:
+            _check(st)
 
 
 def kvq_mixed_sizes(shape):

@@ -537,94 +537,195 @@ kvq_status kvq_append_workspace(const kvq_shape* shape, kvq_dtype x_dtype, const
     return KVQ_OK;
 }
 
-kvq_status kvq_append(const void* x_new, int64_t n, kvq_dtype x_dtype, const kvq_shape* shape, const kvq_qparams* p,
-                      int64_t block, void* codes, void* scale, void* zero, void* resid, int64_t* tq, int64_t* nres,
-                      void* workspace, size_t workspace_B, void* stream)
-{
+namespace {
+
+// One cache of a streaming append: its plan and the caller's buffers.
+struct AppendCache {
     AppendPlan P;
-    kvq_status s = append_plan(shape, x_dtype, p, block, P);
-    if (s != KVQ_OK) return s;
-    if (!tq || !nres) return fail(KVQ_EINVAL, "tq and nres must not be NULL");
-    const int64_t R = p->residual, cap = R + block, Tcap = shape->T;
-    if (n < 0) return fail(KVQ_EINVAL, "n must be >= 0");
-    if (*tq < 0 || *tq % block != 0 || *tq > Tcap)
-        return fail(KVQ_EINVAL, "tq (%lld) must be a multiple of block in [0, T_cap]", (long long)*tq);
-    if (*nres < 0 || *nres >= cap)
-        return fail(KVQ_EINVAL, "nres (%lld) must be in [0, residual + block)", (long long)*nres);
-    // the flushes this call performs, and the store room they need
+    const char* src;            // x_new [outer][n][C]
+    char *codes, *scale, *zero, *resid, *ws;
+    size_t ws_B;
+};
+
+// The flushes an append of n rows performs from the buffer fill nres.
+int64_t append_flushes(int64_t nres, int64_t n, int64_t R, int64_t cap)
+{
     int64_t flushes = 0;
-    for (int64_t cur = *nres, rem = n; rem > 0;) {
+    for (int64_t cur = nres, rem = n; rem > 0;) {
         const int64_t m = std::min(rem, cap - cur);
         cur += m;
         rem -= m;
         if (cur == cap) { ++flushes; cur = R; }
     }
+    return flushes;
+}
+
+// Counters and the store's room for the flushes.
+kvq_status append_counters(const int64_t* tq, const int64_t* nres, int64_t n, int64_t R, int64_t block, int64_t Tcap,
+                           int64_t& flushes)
+{
+    const int64_t cap = R + block;
+    if (!tq || !nres) return fail(KVQ_EINVAL, "tq and nres must not be NULL");
+    if (n < 0) return fail(KVQ_EINVAL, "n must be >= 0");
+    if (*tq < 0 || *tq % block != 0 || *tq > Tcap)
+        return fail(KVQ_EINVAL, "tq (%lld) must be a multiple of block in [0, T_cap]", (long long)*tq);
+    if (*nres < 0 || *nres >= cap)
+        return fail(KVQ_EINVAL, "nres (%lld) must be in [0, residual + block)", (long long)*nres);
+    flushes = append_flushes(*nres, n, R, cap);
     if (*tq + flushes * block > Tcap)
         return fail(KVQ_EINVAL, "the store holds %lld tokens: %lld more would be quantized after %lld",
                     (long long)Tcap, (long long)(flushes * block), (long long)*tq);
+    return KVQ_OK;
+}
+
+// Buffers of one cache: presence, sizes, alignment, workspace.
+kvq_status append_buffers(const AppendCache& c, const kvq_shape* shape, kvq_dtype x_dtype, int64_t n, int64_t cap,
+                          int64_t flushes, const char* who)
+{
+    kvq_status s;
     const size_t es = dtype_bytes(x_dtype);
     const int64_t outer = shape->outer, C = shape->C;
-    const Sizes sz = sizes_of(P.store);
-    if ((s = need_ptr(x_new, (size_t)(outer * n * C) * es, "x_new")) || (s = need_ptr(resid, (size_t)(outer * cap * C) * es, "resid")) ||
-        (flushes && ((s = need_ptr(codes, sz.codes, "codes")) || (s = need_ptr(scale, sz.scale, "scale")) ||
-                     (s = need_ptr(zero, sz.zero, "zero")))))
+    const Sizes sz = sizes_of(c.P.store);
+    if ((s = need_ptr(c.src, (size_t)(outer * n * C) * es, "x_new")) ||
+        (s = need_ptr(c.resid, (size_t)(outer * cap * C) * es, "resid")) ||
+        (flushes && ((s = need_ptr(c.codes, sz.codes, "codes")) || (s = need_ptr(c.scale, sz.scale, "scale")) ||
+                     (s = need_ptr(c.zero, sz.zero, "zero")))))
         return s;
-    if ((s = need_align(x_new, es, "x_new")) || (s = need_align(resid, es, "resid")) ||
-        (s = need_align(scale, dtype_bytes(P.store.scale_dt), "scale")) ||
-        (s = need_align(zero, dtype_bytes(P.store.zero_dt), "zero")) || (s = need_align(workspace, 256, "workspace")))
+    if ((s = need_align(c.src, es, "x_new")) || (s = need_align(c.resid, es, "resid")) ||
+        (s = need_align(c.scale, dtype_bytes(c.P.store.scale_dt), "scale")) ||
+        (s = need_align(c.zero, dtype_bytes(c.P.store.zero_dt), "zero")) || (s = need_align(c.ws, 256, "workspace")))
         return s;
-    if (flushes && (!workspace || workspace_B < P.total))
-        return fail(KVQ_EWORKSPACE, "kvq_append needs %zu workspace bytes (got %zu)", P.total, workspace_B);
+    if (flushes && (!c.ws || c.ws_B < c.P.total))
+        return fail(KVQ_EWORKSPACE, "%s needs %zu workspace bytes (got %zu)", who, c.P.total, c.ws_B);
+    return KVQ_OK;
+}
 
-    cudaStream_t st = (cudaStream_t)stream;
-    char* ws = static_cast<char*>(workspace);
-    char* rbuf = static_cast<char*>(resid);
-    const char* src = static_cast<const char*>(x_new);
+// The append itself for nc caches sharing the counters: one copy launch per
+// buffer segment (every cache's rows together); per flush one quantize per
+// cache and one copy launch for every cache's codes, metadata and kept rows.
+kvq_status append_run(AppendCache* cs, int nc, int64_t n, const kvq_shape* shape, kvq_dtype x_dtype, int64_t R,
+                      int64_t block, int64_t* tq, int64_t* nres, cudaStream_t st, const char* who)
+{
+    const size_t es = dtype_bytes(x_dtype);
+    const int64_t outer = shape->outer, C = shape->C, cap = R + block, Tcap = shape->T;
     const uint64_t rowx = (uint64_t)C * es;                      // bytes of one token row
-    const uint64_t rowc = (uint64_t)C * P.store.bits / 8;        // bytes of one token's codes
     int64_t t = *tq, cur = *nres;
-    kvq::QSpec fq = P.flush;
-    fq.aligned = aligned16(resid) ? 1 : 0;
     for (int64_t j = 0; j < n;) {
         const int64_t m = std::min(n - j, cap - cur);
-        cudaError_t e = kvq::launch_copy2d(rbuf + cur * rowx, cap * rowx, src + j * rowx, n * rowx, m * rowx,
-                                           outer, st);
-        if (e != cudaSuccess) return cuda_status(e, "kvq_append copy");
+        kvq::CopyDesc d[kvq::kMaxCopies];
+        for (int i = 0; i < nc; ++i)
+            d[i] = kvq::CopyDesc{cs[i].resid + cur * rowx, cap * rowx, cs[i].src + j * rowx, n * rowx, m * rowx,
+                                 (uint64_t)outer};
+        cudaError_t e = kvq::launch_copies(d, nc, st);
+        if (e != cudaSuccess) return cuda_status(e, who);
         cur += m;
         j += m;
         if (cur < cap) continue;
         // flush: the oldest `block` rows -> store tokens [t, t + block), the newest R rows -> front of the buffer
-        kvq::QArgs a = {resid, ws + P.off_codes, ws + P.off_scale, ws + P.off_zero, ws + P.off_resid, nullptr,
-                        ws + P.off_qws, P.qws, fq};
-        if ((e = kvq::launch_quantize(a, st)) != cudaSuccess) return cuda_status(e, "kvq_append quantize");
-        e = kvq::launch_copy2d(static_cast<char*>(codes) + t * rowc, Tcap * rowc, ws + P.off_codes, block * rowc,
-                               block * rowc, outer, st);
-        const size_t sb = dtype_bytes(P.store.scale_dt), zb = dtype_bytes(P.store.zero_dt);
-        uint64_t mrow, mpitch, moff;                              // metadata elements per slice and flush
-        if (P.store.axis == KVQ_GROUP_ALONG_T) {
-            mrow = (uint64_t)(block / P.store.g) * C;
-            mpitch = (uint64_t)P.store.ngroups * C;
-            moff = (uint64_t)(t / P.store.g) * C;
-        } else {
-            mrow = (uint64_t)block * P.store.ngroups;
-            mpitch = (uint64_t)Tcap * P.store.ngroups;
-            moff = (uint64_t)t * P.store.ngroups;
+        int nd = 0;
+        for (int i = 0; i < nc; ++i) {
+            AppendCache& c = cs[i];
+            const AppendPlan& P = c.P;
+            kvq::QSpec fq = P.flush;
+            fq.aligned = aligned16(c.resid) ? 1 : 0;
+            kvq::QArgs a = {c.resid, c.ws + P.off_codes, c.ws + P.off_scale, c.ws + P.off_zero, c.ws + P.off_resid,
+                            nullptr, c.ws + P.off_qws, P.qws, fq};
+            if ((e = kvq::launch_quantize(a, st)) != cudaSuccess) return cuda_status(e, who);
+            const uint64_t rowc = (uint64_t)C * P.store.bits / 8;  // bytes of one token's codes
+            const size_t sb = dtype_bytes(P.store.scale_dt), zb = dtype_bytes(P.store.zero_dt);
+            uint64_t mrow, mpitch, moff;                            // metadata elements per slice and flush
+            if (P.store.axis == KVQ_GROUP_ALONG_T) {
+                mrow = (uint64_t)(block / P.store.g) * C;
+                mpitch = (uint64_t)P.store.ngroups * C;
+                moff = (uint64_t)(t / P.store.g) * C;
+            } else {
+                mrow = (uint64_t)block * P.store.ngroups;
+                mpitch = (uint64_t)Tcap * P.store.ngroups;
+                moff = (uint64_t)t * P.store.ngroups;
+            }
+            d[nd++] = kvq::CopyDesc{c.codes + t * rowc, Tcap * rowc, c.ws + P.off_codes, block * rowc, block * rowc,
+                                    (uint64_t)outer};
+            d[nd++] = kvq::CopyDesc{c.scale + moff * sb, mpitch * sb, c.ws + P.off_scale, mrow * sb, mrow * sb,
+                                    (uint64_t)outer};
+            if (P.store.mode == KVQ_ASYM)
+                d[nd++] = kvq::CopyDesc{c.zero + moff * zb, mpitch * zb, c.ws + P.off_zero, mrow * zb, mrow * zb,
+                                        (uint64_t)outer};
+            d[nd++] = kvq::CopyDesc{c.resid, cap * rowx, c.ws + P.off_resid, R * rowx, R * rowx, (uint64_t)outer};
         }
-        if (e == cudaSuccess)
-            e = kvq::launch_copy2d(static_cast<char*>(scale) + moff * sb, mpitch * sb, ws + P.off_scale, mrow * sb,
-                                   mrow * sb, outer, st);
-        if (e == cudaSuccess && P.store.mode == KVQ_ASYM)
-            e = kvq::launch_copy2d(static_cast<char*>(zero) + moff * zb, mpitch * zb, ws + P.off_zero, mrow * zb,
-                                   mrow * zb, outer, st);
-        if (e == cudaSuccess)
-            e = kvq::launch_copy2d(rbuf, cap * rowx, ws + P.off_resid, R * rowx, R * rowx, outer, st);
-        if (e != cudaSuccess) return cuda_status(e, "kvq_append flush");
+        if ((e = kvq::launch_copies(d, nd, st)) != cudaSuccess) return cuda_status(e, who);
         t += block;
         cur = R;
     }
     *tq = t;
     *nres = cur;
     return KVQ_OK;
+}
+
+}  // namespace
+
+kvq_status kvq_append(const void* x_new, int64_t n, kvq_dtype x_dtype, const kvq_shape* shape, const kvq_qparams* p,
+                      int64_t block, void* codes, void* scale, void* zero, void* resid, int64_t* tq, int64_t* nres,
+                      void* workspace, size_t workspace_B, void* stream)
+{
+    AppendCache c;
+    kvq_status s = append_plan(shape, x_dtype, p, block, c.P);
+    if (s != KVQ_OK) return s;
+    int64_t flushes = 0;
+    if ((s = append_counters(tq, nres, n, p->residual, block, shape->T, flushes)) != KVQ_OK) return s;
+    c.src = static_cast<const char*>(x_new);
+    c.codes = static_cast<char*>(codes);
+    c.scale = static_cast<char*>(scale);
+    c.zero = static_cast<char*>(zero);
+    c.resid = static_cast<char*>(resid);
+    c.ws = static_cast<char*>(workspace);
+    c.ws_B = workspace_B;
+    if ((s = append_buffers(c, shape, x_dtype, n, p->residual + block, flushes, "kvq_append")) != KVQ_OK) return s;
+    return append_run(&c, 1, n, shape, x_dtype, p->residual, block, tq, nres, (cudaStream_t)stream, "kvq_append");
+}
+
+kvq_status kvq_append_kv_workspace(const kvq_shape* shape, kvq_dtype x_dtype, const kvq_qparams* k_params,
+                                   const kvq_qparams* v_params, int64_t block, size_t* workspace_B)
+{
+    AppendPlan pk, pv;
+    kvq_status s = append_plan(shape, x_dtype, k_params, block, pk);
+    if (s == KVQ_OK) s = append_plan(shape, x_dtype, v_params, block, pv);
+    if (s != KVQ_OK) return s;
+    if (!workspace_B) return fail(KVQ_EINVAL, "workspace_B must not be NULL");
+    *workspace_B = pk.total + pv.total;
+    return KVQ_OK;
+}
+
+kvq_status kvq_append_kv(const void* k_new, const void* v_new, int64_t n, kvq_dtype x_dtype, const kvq_shape* shape,
+                         const kvq_qparams* k_params, const kvq_qparams* v_params, int64_t block, void* k_codes,
+                         void* k_scale, void* k_zero, void* k_resid, void* v_codes, void* v_scale, void* v_zero,
+                         void* v_resid, int64_t* tq, int64_t* nres, void* workspace, size_t workspace_B, void* stream)
+{
+    AppendCache c[2];
+    kvq_status s = append_plan(shape, x_dtype, k_params, block, c[0].P);
+    if (s == KVQ_OK) s = append_plan(shape, x_dtype, v_params, block, c[1].P);
+    if (s != KVQ_OK) return s;
+    if (k_params->residual != v_params->residual)
+        return fail(KVQ_EINVAL, "K and V share the counters: their residual windows must match (%lld, %lld)",
+                    (long long)k_params->residual, (long long)v_params->residual);
+    int64_t flushes = 0;
+    if ((s = append_counters(tq, nres, n, k_params->residual, block, shape->T, flushes)) != KVQ_OK) return s;
+    const void* src[2] = {k_new, v_new};
+    void* bufs[2][4] = {{k_codes, k_scale, k_zero, k_resid}, {v_codes, v_scale, v_zero, v_resid}};
+    char* ws = static_cast<char*>(workspace);
+    for (int i = 0; i < 2; ++i) {
+        c[i].src = static_cast<const char*>(src[i]);
+        c[i].codes = static_cast<char*>(bufs[i][0]);
+        c[i].scale = static_cast<char*>(bufs[i][1]);
+        c[i].zero = static_cast<char*>(bufs[i][2]);
+        c[i].resid = static_cast<char*>(bufs[i][3]);
+        c[i].ws = ws ? ws + (i ? c[0].P.total : 0) : nullptr;
+        c[i].ws_B = i ? (workspace_B > c[0].P.total ? workspace_B - c[0].P.total : 0)
+                      : std::min(workspace_B, c[0].P.total);
+        if ((s = append_buffers(c[i], shape, x_dtype, n, k_params->residual + block, flushes, "kvq_append_kv")) != KVQ_OK)
+            return s;
+    }
+    return append_run(c, 2, n, shape, x_dtype, k_params->residual, block, tq, nres, (cudaStream_t)stream,
+                      "kvq_append_kv");
 }
 
 namespace {

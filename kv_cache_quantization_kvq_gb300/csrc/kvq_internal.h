@@ -101,9 +101,16 @@ bool rotq_supported(const QSpec& q);
 cudaError_t launch_rotate_quantize(const QArgs& a, const int8_t* signs, cudaStream_t st);
 cudaError_t launch_dequantize_rotate(const QArgs& a, const int8_t* signs, cudaStream_t st);
 
-// ---- strided row copy (append.cu): rows x width bytes, pitches in bytes
-cudaError_t launch_copy2d(void* dst, uint64_t dpitch, const void* src, uint64_t spitch, uint64_t width,
-                          uint64_t rows, cudaStream_t st);
+// ---- strided row copies (append.cu): rows x width bytes, pitches in bytes;
+// up to kMaxCopies independent copies in one launch
+struct CopyDesc {
+    char* dst;
+    uint64_t dpitch;
+    const char* src;
+    uint64_t spitch, width, rows;
+};
+constexpr int kMaxCopies = 8;
+cudaError_t launch_copies(const CopyDesc* d, int n, cudaStream_t st);
 
 // ---- per-token mixed precision (mixed.cu); tags 0..3 = 2/4/8/16 bits, C in {64, 128, 256}
 int64_t mixed_record_bytes(int tag, int64_t C);

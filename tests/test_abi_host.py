@@ -33,7 +33,7 @@ def declared_symbols():
 
 def test_library_exports_every_declared_symbol(kb):
     declared = declared_symbols()
-    assert len(declared) == 25
+    assert len(declared) == 27
     for name in declared:
         assert hasattr(kb.LIB, name), name
     assert declared == set(kb.EXPORTS)
@@ -318,6 +318,39 @@ def test_append_rejected_before_launch(kb):
         with pytest.raises(kb.KvqError) as e:
             call(**kw)
         assert e.value.status == status, (kw, str(e.value))
+
+
+def test_append_kv_rejected_before_launch(kb):
+    """kvq_append_kv: residual windows that differ, bad counters, a store too
+    small, a missing workspace -- rejected, counters unchanged."""
+    import ctypes
+    fake = 1 << 20
+    shape = (2, 256, 128)
+    kq = kb.QParams.asym(4, 0, 15, axis=kb.ALONG_T, group=64, residual=128, scale_dtype=kb.BF16, zero_dtype=kb.BF16)
+    vq = kb.QParams.asym(4, 0, 15, axis=kb.ALONG_C, group=64, residual=128, scale_dtype=kb.BF16, zero_dtype=kb.BF16)
+    v_other = kb.QParams.asym(4, 0, 15, axis=kb.ALONG_C, group=64, residual=64, scale_dtype=kb.BF16, zero_dtype=kb.BF16)
+    wB = kb.kvq_append_kv_workspace(shape, kb.BF16, kq, vq, 64)
+    assert wB == kb.kvq_append_workspace(shape, kb.BF16, kq, 64) + kb.kvq_append_workspace(shape, kb.BF16, vq, 64)
+    bufs = (fake, fake, fake, fake)
+    for kw, status in (
+            (dict(vqp=v_other), kb.EINVAL),                          # residual windows differ
+            (dict(tq=3), kb.EINVAL),                                 # tq not a multiple of block
+            (dict(nres=192), kb.EINVAL),                             # nres = residual + block
+            (dict(n=-1), kb.EINVAL),
+            (dict(tq=256, nres=191, n=1), kb.EINVAL),                # the flush does not fit the store
+            (dict(nres=191, n=1, ws=None, wsB=0), kb.EWORKSPACE),    # a flush without workspace
+            (dict(nres=191, n=1, wsB=wB - 1), kb.EWORKSPACE),
+            (dict(k_new=None), kb.EINVAL),
+            (dict(v_new=fake + 1), kb.EINVAL)):                      # misaligned bf16 rows
+        a = dict(k_new=fake, v_new=fake, n=1, vqp=vq, tq=0, nres=0, ws=fake, wsB=wB)
+        a.update(kw)
+        t, r = ctypes.c_int64(a["tq"]), ctypes.c_int64(a["nres"])
+        with pytest.raises(kb.KvqError) as e:
+            kb._check(kb.LIB.kvq_append_kv(a["k_new"], a["v_new"], a["n"], kb.BF16, ctypes.byref(kb._shape(shape)),
+                                           ctypes.byref(kq.c()), ctypes.byref(a["vqp"].c()), 64, *bufs, *bufs,
+                                           ctypes.byref(t), ctypes.byref(r), a["ws"], a["wsB"], None))
+        assert e.value.status == status, (kw, str(e.value))
+        assert (t.value, r.value) == (a["tq"], a["nres"]), kw
 
 
 def test_mixed_rejected_before_launch(kb):

@@ -113,3 +113,63 @@ def test_append_matches_whole_sequence_quantize(b, case):
 
 def test_append_state_after_every_chunk(b):
     run(b, (4, (0, 15), O.ALONG_T, 16, 8, 16, 64, 2, 120), check_every=True)
+
+
+# K and V of one layer through one kvq_append_kv call per chunk: each cache
+# must end exactly as if quantized whole (and as kvq_append leaves it).
+KV_CASES = [
+    # K (bits, (qmin, qmax), g), V (bits, (qmin, qmax), g), R, block, C, outer, T, chunk sizes
+    ((4, (0, 15), 64), (4, (0, 15), 64), 128, 64, 128, 3, 700, "decode"),      # KIVI formats, one token a step
+    ((4, (0, 15), 32), (4, (0, 15), 64), 16, 32, 128, 2, 300, "random"),
+    ((8, None, 16), (2, None, 32), 40, 48, 64, 2, 400, "random"),
+    ((4, (0, 15), 64), (4, (0, 15), 64), 128, 64, 128, 2, 150, "random"),      # nothing flushed
+]
+
+
+def _formats(spec, axis, R):
+    bits, qr, g = spec
+    if qr is None:
+        return O.QParams.sym(bits, axis=axis, group=g, residual=R, scale_dtype=O.BF16 if bits < 8 else O.F32)
+    return O.QParams.asym(bits, qr[0], qr[1], axis=axis, group=g, residual=R, scale_dtype=O.BF16, zero_dtype=O.BF16)
+
+
+@pytest.mark.parametrize("case", KV_CASES, ids=str)
+def test_append_kv_matches_whole_sequence_quantize(b, case):
+    import torch
+    kspec, vspec, R, block, C, outer, T, chunks = case
+    rng = np.random.default_rng(zlib.crc32(repr(case).encode()))
+    X = {n: W.to_bf16_bits(W.random_kv(rng, (outer, T, C))) for n in ("K", "V")}
+    oq = {"K": _formats(kspec, O.ALONG_T, R), "V": _formats(vspec, O.ALONG_C, R)}
+    kq = {n: kq_of(b, oq[n]) for n in oq}
+    shape = (outer, T, C)
+    g = Guarded()
+    bufs = {}
+    for n in ("K", "V"):
+        q0 = kq[n]
+        cB, sB, zB, _, _ = b.kvq_quantized_sizes(shape, b.BF16, b.QParams(q0.bits, q0.mode, q0.qmin, q0.qmax, q0.axis,
+                                                                          q0.group, 0, q0.scale_dtype, q0.zero_dtype))
+        bufs[n] = (g.alloc(max(cB, 1), fill=0), g.alloc(max(sB, 1), fill=0), g.alloc(max(zB, 1), fill=0),
+                   g.alloc(outer * (R + block) * C * 2, fill=0).view(torch.bfloat16))
+    wB = b.kvq_append_kv_workspace(shape, b.BF16, kq["K"], kq["V"], block)
+    ws = g.alloc(max(wB, 1))
+    Xd = {n: torch.from_numpy(X[n].view(np.int16)).view(torch.bfloat16).cuda() for n in X}
+    app = b.KVAppender(shape, b.BF16, kq["K"], kq["V"], block, bufs["K"], bufs["V"], ws)
+    t, step = 0, 0
+    tq, nres = 0, 0
+    while t < T:
+        n = 1 if chunks == "decode" else int(min(T - t, rng.integers(1, 70)))
+        n = min(n, T - t)
+        kc, vc = Xd["K"][:, t:t + n].contiguous(), Xd["V"][:, t:t + n].contiguous()
+        if step % 2:      # the object and the plain call alternate on the same counters
+            app = b.KVAppender(shape, b.BF16, kq["K"], kq["V"], block, bufs["K"], bufs["V"], ws, tq=tq, nres=nres)
+            app.append(kc, vc, n)
+            tq, nres = app.tq, app.nres
+        else:
+            tq, nres = b.kvq_append_kv(kc, vc, n, b.BF16, shape, kq["K"], kq["V"], block, bufs["K"], bufs["V"], tq,
+                                       nres, ws, wB)
+        t += n
+        step += 1
+    g.check("kvq_append_kv")
+    for n in ("K", "V"):
+        codes, scale, zero, resid = bufs[n]
+        compare(b, X[n], oq[n], tq, nres, codes, scale, zero, resid, R, block)
