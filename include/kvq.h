@@ -359,7 +359,8 @@ KVQ_API kvq_status kvq_append_kv(const void* k_new, const void* v_new, int64_t n
  *  - tags2[o][ceil(T/4)]: the 2-bit tags, token t at bit 2*(t%4) of byte t/4.
  * Scales and zero points are rounded to bf16 before the codes are computed,
  * exactly as the uniform quantizer does.
- *  - x, out: bf16; C must be 64, 128 or 256 (KVQ_EUNSUPPORTED otherwise).
+ *  - x, out: bf16; x, out and stream_buf 16-byte aligned, off 8-byte aligned;
+ *    C must be 64, 128 or 256 (KVQ_EUNSUPPORTED otherwise).
  *  - Sizes: kvq_mixed_sizes (stream bytes are those of the all-16-bit case;
  *    off[o][T] tells how many a slice really uses).
  *  - Errors: KVQ_EINVAL (NULL or misaligned buffers), KVQ_ECUDA. */

@@ -783,6 +783,7 @@ kvq_status kvq_mixed_quantize(const void* x, const uint8_t* tags, const kvq_shap
         return s;
     if ((s = need_align(x, 2, "x")) || (s = need_align(stream_buf, 2, "stream_buf")) || (s = need_align(off, 8, "off")))
         return s;
+    if (!aligned16(x) || !aligned16(stream_buf)) return fail(KVQ_EINVAL, "x and stream_buf must be 16-byte aligned");
     const kvq::QSpec f2 = mixed_format(2, shape->C), f4 = mixed_format(4, shape->C), f8 = mixed_format(8, shape->C);
     return cuda_status(kvq::launch_mixed_quantize(x, tags, shape->outer, shape->T, shape->C, stream_buf, off, tags2,
                                                   f2, f4, f8, (cudaStream_t)stream),
@@ -800,6 +801,7 @@ kvq_status kvq_mixed_dequantize(const void* stream_buf, const int64_t* off, cons
         return s;
     if ((s = need_align(stream_buf, 2, "stream_buf")) || (s = need_align(off, 8, "off")) || (s = need_align(out, 2, "out")))
         return s;
+    if (!aligned16(out) || !aligned16(stream_buf)) return fail(KVQ_EINVAL, "out and stream_buf must be 16-byte aligned");
     return cuda_status(kvq::launch_mixed_dequantize(stream_buf, off, tags2, shape->outer, shape->T, shape->C, out,
                                                     (cudaStream_t)stream),
                        "kvq_mixed_dequantize launch");

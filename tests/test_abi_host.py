@@ -357,11 +357,17 @@ def test_mixed_rejected_before_launch(kb):
     fake = 1 << 20
     assert kb.kvq_mixed_sizes((2, 10, 128)) == (2 * 10 * 128 * 2, 2 * 11 * 8, 2 * 3)
     for shape, x, off, status in (((2, 10, 96), fake, fake, kb.EUNSUPPORTED), ((2, 10, 128), None, fake, kb.EINVAL),
-                                  ((2, 10, 128), fake + 1, fake, kb.EINVAL), ((2, 10, 128), fake, fake + 4, kb.EINVAL)):
+                                  ((2, 10, 128), fake + 1, fake, kb.EINVAL), ((2, 10, 128), fake, fake + 4, kb.EINVAL),
+                                  ((2, 10, 128), fake + 2, fake, kb.EINVAL)):     # rows read 16 bytes at a time
         with pytest.raises(kb.KvqError) as e:
             kb.kvq_mixed_quantize(x, fake, shape, fake, off, fake, 0)
         assert e.value.status == status, (shape, str(e.value))
-    with pytest.raises(kb.KvqError) as e:
-        kb.kvq_mixed_dequantize(fake, fake, fake, (2, 10, 128), None, 0)
-    assert e.value.status == kb.EINVAL
+    for shape, x, off, status in (((2, 10, 128), fake, fake, kb.EINVAL),):       # stream_buf by bulk copies
+        with pytest.raises(kb.KvqError) as e:
+            kb.kvq_mixed_quantize(x, fake, shape, fake + 2, off, fake, 0)
+        assert e.value.status == status, (shape, str(e.value))
+    for sbuf, out in ((fake, None), (fake, fake + 2), (fake + 2, fake)):
+        with pytest.raises(kb.KvqError) as e:
+            kb.kvq_mixed_dequantize(sbuf, fake, fake, (2, 10, 128), out, 0)
+        assert e.value.status == kb.EINVAL
 

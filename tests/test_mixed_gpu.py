@@ -120,8 +120,9 @@ def test_mixed_random_tags(b, C):
 
 
 def test_mixed_random_tags_long_slices(b):
-    """Thousands of tokens per slice: each thread of the offset scan sums a
-    segment of 20 tokens, the last one ragged (5003 = 250 * 20 + 3)."""
+    """Thousands of tokens per slice at C = 64: 20 sub-rounds of 256 tokens,
+    one per CTA, the last one ragged (5003 = 19 * 256 + 139); every CTA but the
+    first sums the record bytes of the tokens before it."""
     rng = np.random.default_rng(5003)
     shape = (2, 5003, 64)
     run(b, shape, rng.integers(0, 4, shape[:2]), seed=11)
@@ -129,8 +130,8 @@ def test_mixed_random_tags_long_slices(b):
 
 @pytest.mark.parametrize("tag", [0, 1, 2])
 def test_mixed_one_level_beyond_one_grid_pass(b, tag):
-    """More token rows than one pass of the capped grid covers, so every warp
-    loops; a 784-token scan segment per thread with a ragged end."""
+    """200003 tokens in one slice: 32 CTAs of 49 sub-rounds of 128 tokens
+    each, the last one ragged; record offsets beyond 2^24 bytes."""
     T = 200003
     shape = (1, T, 128)
     run(b, shape, np.full(shape[:2], tag), seed=tag + 20, one_level=tag)
