@@ -306,6 +306,13 @@ def run_ours(args, rank, world, local_rank):
         return {"metric": METRIC, "unit": UNIT, "n_gpus": 1, "data": "synthetic",
                 "config": {"workload": "kivi_int4 decode attention [b8,h8,T8192,d128,g64,R128]", "only": "attend"},
                 "configs": run_configs(b, dev, stream, flush, only_attend=True)}
+    if args.only == "rotate":
+        # the rotation rows alone (profiling)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+        return {"metric": METRIC, "unit": UNIT, "n_gpus": 1, "data": "synthetic",
+                "config": {"workload": "kivi_int4 rotation [b8,h8,T8192,d128]", "only": "rotate"},
+                "configs": run_configs(b, dev, stream, flush, only_rotate=True)}
     if args.only == "fullmodel":
         # the full-model INT8 rows alone (profiling; --fullmodel-layers shrinks the case)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -528,12 +535,15 @@ def quant_bytes(shape, x_es, cB, sB, zB, rB):
     return x + cB + sB + zB + rB, x + cB + sB + zB
 
 
-def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32, only_attend=False):
+def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32, only_attend=False,
+                only_rotate=False):
     """Median over `runs` (L2 flushed before each) of every op of the large
     configurations: KIVI INT4 (2), full-model INT8 per channel (3), the
     group / bit-width sweep (4), H2O / SnapKV (5); the tiny one (1) in us.
     only_fullmodel: the full-model rows alone, with `layers` layers;
-    only_attend: the fused decode attention over the KIVI cache alone."""
+    only_attend: the fused decode attention over the KIVI cache alone;
+    only_rotate: the rotation rows (stand-alone, and fused into the value
+    cache's quantize / dequantize) alone."""
     import torch
     from kv_cache_quantization_kvq_gb300 import workloads as W
     peak, _ = measured_peak()
@@ -582,6 +592,28 @@ def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32,
         return out
     # 2: KIVI INT4
     K, V = W.kivi_kv(dev, seed=2)
+
+    def rotate_rows():
+        # randomized Hadamard rotation of the key cache (bf16 -> bf16): read + write
+        signs = torch.where(torch.rand(K.shape[-1], device=dev, generator=torch.Generator(device=dev).manual_seed(3)) < 0.5,
+                            -1, 1).to(torch.int8)
+        rot = torch.empty_like(K)
+        out["2_kivi_int4/K/rotate"] = entry(med(lambda: b.rotate(K, signs, out=rot, stream=stream)), 2 * K.numel() * 2)
+        # the rotation fused into the value cache's per-token quantize and dequantize
+        # (the KIVI value format): the same bytes as the plain quantize / dequantize
+        vqf = b.QParams.asym(4, 0, 15, axis=b.ALONG_C, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
+        qvf, _ = b.alloc_quantized(tuple(V.shape), b.BF16, vqf, dev)
+        fq_B, _ = quant_bytes(tuple(V.shape), 2, *(t.numel() for t in (qvf.codes, qvf.scale, qvf.zero, qvf.resid)))
+        vout = torch.empty_like(V)
+        out["2_kivi_int4/V/rotate_quantize"] = entry(med(lambda: b.rotate_quantize(V, signs, vqf, out=qvf, stream=stream)),
+                                                     fq_B)
+        out["2_kivi_int4/V/dequantize_rotate"] = entry(med(lambda: b.dequantize_rotate(qvf, signs, out=vout, stream=stream)),
+                                                       fq_B)
+        del rot, qvf, vout
+
+    if only_rotate:
+        rotate_rows()
+        return out
     if not only_attend:
         for axis, x, name in ((b.ALONG_T, K, "K"), (b.ALONG_C, V, "V")):
             qp = b.QParams.asym(4, 0, 15, axis=axis, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
@@ -647,22 +679,8 @@ def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32,
                                                   used + oB + tB + K.numel() * 2)
     out["2_kivi_int4/K/mixed_bytes_per_number"] = round((used + tB) / K.numel(), 6)
     del mbuf, moff, mt2, mout, tags
-    # randomized Hadamard rotation of the key cache (bf16 -> bf16): read + write
-    signs = torch.where(torch.rand(K.shape[-1], device=dev, generator=torch.Generator(device=dev).manual_seed(3)) < 0.5,
-                        -1, 1).to(torch.int8)
-    rot = torch.empty_like(K)
-    out["2_kivi_int4/K/rotate"] = entry(med(lambda: b.rotate(K, signs, out=rot, stream=stream)), 2 * K.numel() * 2)
-    # the rotation fused into the value cache's per-token quantize and dequantize
-    # (the KIVI value format): the same bytes as the plain quantize / dequantize
-    vqf = b.QParams.asym(4, 0, 15, axis=b.ALONG_C, group=64, residual=128, scale_dtype=b.BF16, zero_dtype=b.BF16)
-    qvf, _ = b.alloc_quantized(tuple(V.shape), b.BF16, vqf, dev)
-    fq_B, _ = quant_bytes(tuple(V.shape), 2, *(t.numel() for t in (qvf.codes, qvf.scale, qvf.zero, qvf.resid)))
-    vout = torch.empty_like(V)
-    out["2_kivi_int4/V/rotate_quantize"] = entry(med(lambda: b.rotate_quantize(V, signs, vqf, out=qvf, stream=stream)),
-                                                 fq_B)
-    out["2_kivi_int4/V/dequantize_rotate"] = entry(med(lambda: b.dequantize_rotate(qvf, signs, out=vout, stream=stream)),
-                                                   fq_B)
-    del K, V, rot, qvf, vout
+    rotate_rows()
+    del K, V
     # 3: full model INT8, per channel over all tokens
     K, V = W.fullmodel_kv(dev, seed=3)
     qdq("3_fullmodel_int8", [("K", K), ("V", V)], b.QParams.sym(8, axis=b.ALONG_T, group=0))
@@ -983,10 +1001,10 @@ def main():
                          "branches of the step graph")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue the timed steps as plain C-ABI calls instead of replaying a captured CUDA graph")
-    ap.add_argument("--only", choices=("all", "kivi", "evict", "fullmodel", "attend"), default="all",
+    ap.add_argument("--only", choices=("all", "kivi", "evict", "fullmodel", "attend", "rotate"), default="all",
                     help="time only the KIVI phases or only the eviction phases (profiling); "
-                         "fullmodel / attend: only the full-model INT8 rows / the fused decode-attention "
-                         "rows of the per-configuration table")
+                         "fullmodel / attend / rotate: only the full-model INT8 rows / the fused decode-attention "
+                         "rows / the rotation rows of the per-configuration table")
     ap.add_argument("--fullmodel-layers", type=int, default=32,
                     help="layers of the full-model INT8 workload with --only fullmodel (a smaller profiling case)")
     ap.add_argument("--evict-tokens", type=int, default=None,
