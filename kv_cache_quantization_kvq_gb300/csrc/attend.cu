@@ -360,9 +360,11 @@ attend_split_kernel(const AttnArgs a)
 //    so the probabilities never leave registers: Y[16 x 128] = P'[16 x 16] .
 //    V[16 x 128] with P' = p * s_v(token, V group) split hi / lo the same
 //    way and V the value fields minus (off + zp) per token.
-//  * A tile holding residual tokens, tokens past T, or a group whose zero
-//    points bf16 cannot hold exactly takes a float32 scalar path with the
-//    same register layout (exact products, one FMA each).
+//  * A tile whose tokens are all residual (or past T) takes the same two
+//    products with the bf16 rows as operands; a tile straddling the
+//    quantized / residual boundary, or a group whose zero points bf16 cannot
+//    hold exactly, takes a float32 scalar path with the same register layout
+//    (exact products, one FMA each).
 // The online softmax, the merge of the warps of a CTA and the split
 // partials are those of the scalar kernel above.
 constexpr int kTcTile = 16;
