@@ -4,9 +4,12 @@ time, in a fresh process (so no kernel attribute has been set yet).
 The launchers that need more than 48 KB of dynamic shared memory raise that
 limit once per (device, kernel) under a lock.  Both threads race through
 those first launches -- the warp-specialised quantize kernels (groups along T
-and along C), the warp-specialised dequantize / statistics kernel, the
-cluster quantize kernel and the fused selection kernel -- each on its own
-stream, and every result must still equal the CPU oracle bit for bit.
+and along C), the warp-specialised dequantize / statistics kernel, both forms
+of the cluster quantize kernel (all rows in shared memory; half of them in
+registers for groups over 2048 tokens), the fused selection kernel, the
+mixed-precision kernels and the tensor-core attention kernel -- each on its
+own stream.  Every result must still equal the CPU oracle bit for bit, and the
+two threads' attention outputs must be identical.
 """
 import os
 import subprocess
@@ -35,11 +38,15 @@ CHILD = textwrap.dedent(r"""
     rng = np.random.default_rng(0)
     xk = W.to_bf16_bits(W.random_kv(rng, (4, 301, 128)))
     xl = W.to_bf16_bits(W.random_kv(rng, (2, 1100, 128)))
+    xr = W.to_bf16_bits(W.random_kv(rng, (1, 2600, 128)))
+    xm = W.to_bf16_bits(W.random_kv(rng, (2, 300, 128)))
+    tags = rng.integers(0, 4, (2, 300)).astype(np.uint8)
     hist = W.random_history(rng, 3, 5, 5000, planted=16)
     fmts = [
         (xk, O.QParams.asym(4, 0, 15, axis=O.ALONG_T, group=64, residual=13, scale_dtype=O.BF16, zero_dtype=O.BF16)),
         (xk, O.QParams.asym(4, 0, 15, axis=O.ALONG_C, group=64, residual=13, scale_dtype=O.BF16, zero_dtype=O.BF16)),
         (xl, O.QParams.sym(8, axis=O.ALONG_T, group=0)),
+        (xr, O.QParams.sym(8, axis=O.ALONG_T, group=0)),
     ]
     want = [(O.quantize(x, O.BF16, q), O.dequantize(O.quantize(x, O.BF16, q), x.shape, q, O.BF16),
              O.error_stats(x, O.BF16, O.quantize(x, O.BF16, q), q)) for x, q in fmts]
@@ -47,10 +54,21 @@ CHILD = textwrap.dedent(r"""
     torch.cuda.set_device(0)
     dev_in = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for x, _ in fmts]
     hd = torch.from_numpy(hist).cuda()
+    xmd = torch.from_numpy(xm.view(np.int16)).view(torch.bfloat16).cuda()
+    tgd = torch.from_numpy(tags).cuda()
+    # the mixed-precision reference: one thread's single-threaded result is
+    # checked against the oracle by test_mixed_gpu; here both racing threads
+    # must reproduce a result computed before the race
+    msB, moB, mtB = b.kvq_mixed_sizes(tuple(xm.shape))
+    kq8 = kq_of(b, O.QParams.asym(4, 0, 15, axis=O.ALONG_T, group=64, residual=128, scale_dtype=O.BF16, zero_dtype=O.BF16))
+    vq8 = kq_of(b, O.QParams.asym(4, 0, 15, axis=O.ALONG_C, group=64, residual=128, scale_dtype=O.BF16, zero_dtype=O.BF16))
+    qk8, qv8 = b.quantize(dev_in[0][:, :256].contiguous(), kq8), b.quantize(dev_in[1][:, :256].contiguous(), vq8)
+    q8 = torch.randn((4, 8, 128), device="cuda", generator=torch.Generator(device="cuda").manual_seed(1))
     torch.cuda.synchronize()
 
     gate = threading.Barrier(2)
     errors = []
+    results = {}
 
     def worker(tid):
         try:
@@ -65,7 +83,15 @@ CHILD = textwrap.dedent(r"""
                     st = b.error_stats(xd, qt, stream=s)
                     outs.append((qt, xh, st))
                 keep, _ = b.h2o_select(hd, 300, 32, stream=s)
+                mbuf = torch.empty(msB, dtype=torch.uint8, device="cuda")
+                moff = torch.empty(moB // 8, dtype=torch.int64, device="cuda")
+                mt2 = torch.empty(mtB, dtype=torch.uint8, device="cuda")
+                mout = torch.empty_like(xmd)
+                b.kvq_mixed_quantize(xmd, tgd, tuple(xm.shape), mbuf, moff, mt2, s)
+                b.kvq_mixed_dequantize(mbuf, moff, mt2, tuple(xm.shape), mout, s)
+                att = b.attend_decode(q8, qk8, qv8, stream=s)
             s.synchronize()
+            results[tid] = (to_host(mbuf), to_host(moff), to_host(mout), att.cpu().numpy())
             for (qt, xh, st), (wq, wd, ws), (x, q) in zip(outs, want, fmts):
                 assert np.array_equal(to_host(qt.codes), wq.codes), f"thread {tid}: codes"
                 assert np.array_equal(to_host(xh).reshape(x.shape), wd), f"thread {tid}: dequantized values"
@@ -81,6 +107,14 @@ CHILD = textwrap.dedent(r"""
         t.join(timeout=600)
     assert not any(t.is_alive() for t in ts), "a thread did not finish"
     assert not errors, errors
+    r0, r1 = results[0], results[1]
+    offs = r0[1].reshape(2, 301)
+    assert np.array_equal(r0[1], r1[1]), "threads differ in the record offsets"
+    for o in range(2):                          # each slice's records up to the bytes it uses
+        n = int(offs[o, -1])
+        assert np.array_equal(r0[0].reshape(2, -1)[o, :n], r1[0].reshape(2, -1)[o, :n]), "threads differ in records"
+    assert np.array_equal(r0[2], r1[2]), "threads differ in the mixed dequantized values"
+    assert np.array_equal(r0[3], r1[3]), "threads differ in the attention output"
     assert b.kvq_wait_timeouts() == 0
     print("threads: ok")
 """)
