@@ -26,6 +26,7 @@
 #include <algorithm>
 #include <cmath>
 
+#include "kvq_div.cuh"
 #include "kvq_elem.cuh"
 
 namespace kvq {
@@ -44,32 +45,6 @@ __device__ __forceinline__ uint4 ld_once16(const void* p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
-}
-
-// n / d for 32-bit n by a multiply-high and shifts (d >= 1 fixed per launch):
-// with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
-// n / d = (t + ((n - t) >> 1)) >> (l - 1), t = mulhi(m, n), for every 32-bit
-// n (Granlund and Montgomery, "Division by invariant integers using
-// multiplication", 1994, section 4); d = 1 is taken apart.
-struct DivU32 {
-    uint32_t d, m, sh;
-};
-
-DivU32 make_div(uint32_t d) {
-    DivU32 v{d, 0u, 0u};
-    if (d > 1) {
-        uint32_t l = 0;
-        while ((1ull << l) < d) ++l;
-        v.m = (uint32_t)(((1ull << 32) * ((1ull << l) - d)) / d + 1);
-        v.sh = l - 1;
-    }
-    return v;
-}
-
-__device__ __forceinline__ uint32_t div_u32(uint32_t n, const DivU32& v) {
-    if (v.d == 1) return n;
-    const uint32_t t = __umulhi(v.m, n);
-    return (t + ((n - t) >> 1)) >> v.sh;
 }
 
 // Sign masks of the C/2 bf16 pairs of a row in shared memory (bit 15 / 31
