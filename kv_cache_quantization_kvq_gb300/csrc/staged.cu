@@ -1220,25 +1220,24 @@ wds_t_kernel(const QArgs a, Partial* partials, unsigned int* done, kvq_err* out_
 }
 
 // ======================================================================
-// dequantize / statistics along C, warp-specialised (bf16, C = 128, groups of
-// 32, 64 or 128 channels per token).  A chunk is kDcRows consecutive
-// quantized token rows of one slice: the producer warp bulk-copies their codes
-// (and, for the statistics, the source rows) into a ring stage; the group
-// constants belong to each token, so every lane loads the scale and zero point
-// of its rows' group straight from global memory at the start of the tile,
-// all loads in flight together.  Teams, stages, lane mapping, residual copy and
-// the fused final reduction are those of wds_t_kernel.
+// dequantize along C, warp-specialised (bf16, C = 128, groups of 32, 64 or
+// 128 channels per token).  A chunk is kDcRows consecutive quantized token
+// rows of one slice: the producer warp bulk-copies their codes into a ring
+// stage (and the codes one ring-length ahead into L2); the group constants
+// belong to each token, so every lane loads the scale and zero point of its
+// rows' group straight from global memory before it waits on the tile, all
+// loads in flight together.  Teams, stages, lane mapping and the residual
+// copy are those of wds_t_kernel.  (The statistics along C stay on ds_kernel:
+// this form of them measured slower.)
 // ======================================================================
 constexpr int kDcRows = 64;
 
-template <int BITS, bool STATS>
+template <int BITS>
 struct DcShape {
     static constexpr int CR = kDcRows;
-    static constexpr uint32_t kXB = STATS ? (uint32_t)CR * 256u : 0u;  // the source rows (statistics)
-    static constexpr int WT = STATS ? 4 : 2;
+    static constexpr int WT = 2;                                      // consumer warps sharing one stage
     static constexpr uint32_t kCodeRowB = 16u * BITS;
-    static constexpr uint32_t offCodes = kXB;
-    static constexpr uint32_t kStage = (kXB + (uint32_t)CR * kCodeRowB + 127u) / 128u * 128u;
+    static constexpr uint32_t kStage = ((uint32_t)CR * kCodeRowB + 127u) / 128u * 128u;
     static constexpr int kConsumers = 16;
     static constexpr int kTeams = kConsumers / WT;
     static constexpr int kStages = 2 * kTeams;
@@ -1247,11 +1246,11 @@ struct DcShape {
     static_assert(kSmem <= 227 * 1024, "ring does not fit in shared memory");
 };
 
-template <int BITS, bool ASYM, int G, bool STATS, int SDT, int ZDT>
-__global__ void __launch_bounds__(DcShape<BITS, STATS>::kThreads, 1)
-wds_c_kernel(const QArgs a, Partial* partials, unsigned int* done, kvq_err* out_dev)
+template <int BITS, bool ASYM, int G, int SDT, int ZDT>
+__global__ void __launch_bounds__(DcShape<BITS>::kThreads, 1)
+wds_c_kernel(const QArgs a)
 {
-    using L = DcShape<BITS, STATS>;
+    using L = DcShape<BITS>;
     using W = typename CodeWord<BITS>::T;
     constexpr int C = 128, NG = C / G, CR = L::CR;
     constexpr int P = L::kTeams, S = L::kStages, WT = L::WT, NCW = L::kConsumers;
@@ -1292,19 +1291,14 @@ wds_c_kernel(const QArgs a, Partial* partials, unsigned int* done, kvq_err* out_
             if (n >= (uint32_t)S && !mbar_wait(&empty[s], ((n / S) - 1) & 1u)) break;
             uint32_t o, row0, nrows;
             geom(c, o, row0, nrows);
-            unsigned char* st = smem + s * L::kStage;
-            mbar_expect_tx(&full[s], nrows * (L::kXB ? 256u : 0u) + nrows * L::kCodeRowB);
-            if (STATS)
-                bulk_g2s(st, static_cast<const __nv_bfloat16*>(a.x) + ((uint64_t)o * T32 + row0) * C, nrows * 256u, &full[s]);
-            bulk_g2s(st + L::offCodes, codes + ((uint64_t)o * Tq32 + row0) * L::kCodeRowB, nrows * L::kCodeRowB, &full[s]);
-            if (!STATS) {
-                // the codes one ring-length ahead into L2
-                const uint32_t cq = c + (uint32_t)S * step;
-                if (cq < nchunks && cq > c) {
-                    uint32_t po, prow0, pn;
-                    geom(cq, po, prow0, pn);
-                    bulk_prefetch_l2(codes + ((uint64_t)po * Tq32 + prow0) * L::kCodeRowB, pn * L::kCodeRowB);
-                }
+            mbar_expect_tx(&full[s], nrows * L::kCodeRowB);
+            bulk_g2s(smem + s * L::kStage, codes + ((uint64_t)o * Tq32 + row0) * L::kCodeRowB, nrows * L::kCodeRowB,
+                     &full[s]);
+            const uint32_t cq = c + (uint32_t)S * step;        // the codes one ring-length ahead into L2
+            if (cq < nchunks && cq > c) {
+                uint32_t po, prow0, pn;
+                geom(cq, po, prow0, pn);
+                bulk_prefetch_l2(codes + ((uint64_t)po * Tq32 + prow0) * L::kCodeRowB, pn * L::kCodeRowB);
             }
         }
         for (uint32_t i = n > (uint32_t)S ? n - S : 0; i < n; ++i) mbar_wait(&full[i % S], (i / S) & 1u);
@@ -1319,7 +1313,8 @@ wds_c_kernel(const QArgs a, Partial* partials, unsigned int* done, kvq_err* out_
     const int chan0 = c8 * 8, grp = chan0 / G;
     const int off = q.is_signed ? (1 << (BITS - 1)) : 0;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    Acc2 A;
+    TileAcc ta;                                             // unused: dequantize only
+    uint32_t mxb = 0;
     for (uint32_t j = pair;; j += P) {
         const uint32_t c = first + j * step;
         if (c >= nchunks) break;
@@ -1336,19 +1331,15 @@ wds_c_kernel(const QArgs a, Partial* partials, unsigned int* done, kvq_err* out_
             zr[i] = ASYM ? ld_meta<ZDT>(a.zero, mi) : 0.0f;
         }
         const int s = (int)(j % S);
-        // on a timeout (recorded in g_kvq_wait_timeouts) leave the loop but still reach the barriers below
+        // on a timeout (recorded in g_kvq_wait_timeouts) leave the loop
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (j / S) & 1u))) break;
-        const unsigned char* st = smem + s * L::kStage;
-        const unsigned char* cbase = st + L::offCodes + (uint32_t)c8 * BITS;
-        const unsigned char* xbase = st + chan0 * 2;
+        const unsigned char* cbase = smem + s * L::kStage + (uint32_t)c8 * BITS;
         __nv_bfloat16* obase = out + ((uint64_t)o * T32 + row0) * C + chan0;
-        TileAcc ta;
 #pragma unroll
         for (int i = 0; i < NR; ++i) {                     // fully unrolled: sr / zr stay in registers
             const int r = rq + RSTEP * i;
             if (r < nrows) {
                 const W cw = *reinterpret_cast<const W*>(cbase + (uint32_t)r * L::kCodeRowB);
-                const uint4 xw = STATS ? *reinterpret_cast<const uint4*>(xbase + (uint32_t)r * 256u) : make_uint4(0, 0, 0, 0);
                 uint32_t u[8];
                 unpack_biased8<BITS>(q.is_signed ? flip_signs<BITS>(cw) : cw, u);
                 uint4 ow;
@@ -1356,69 +1347,29 @@ wds_c_kernel(const QArgs a, Partial* partials, unsigned int* done, kvq_err* out_
                     u64 c1, s1;
                     dq_pair_consts(sr[i], zr[i], off, c1, s1);
                     const u64 cp[4] = {c1, c1, c1, c1}, sp[4] = {s1, s1, s1, s1};
-                    ow = dq8<STATS>(u, cp, sp, xw, ta, A.mxb);
+                    ow = dq8<false>(u, cp, sp, make_uint4(0, 0, 0, 0), ta, mxb);
                 } else {
                     // exact reference order for groups with a very large zero point
                     float sf[8], zf[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) { sf[k] = sr[i]; zf[k] = zr[i]; }
-                    ow = dq8_slow<STATS>(u, off, zf, sf, xw, ta, A.mxb);
+                    ow = dq8_slow<false>(u, off, zf, sf, make_uint4(0, 0, 0, 0), ta, mxb);
                 }
-                if (!STATS) *reinterpret_cast<uint4*>(obase + (uint64_t)r * C) = ow;
+                *reinterpret_cast<uint4*>(obase + (uint64_t)r * C) = ow;
             }
         }
-        if (STATS) A.fold(ta);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
 
+    // residual rows: resid [outer][R][C] -> out rows Tq .. T-1, 16 bytes per item
     constexpr int kCons = NCW * 32;                        // consumer threads
-    if (!STATS) {
-        // residual rows: resid [outer][R][C] -> out rows Tq .. T-1, 16 bytes per item
-        const uint64_t nres = (uint64_t)q.outer * (uint64_t)q.R * (C / 8);
-        const uint4* rs = static_cast<const uint4*>(a.resid);
-        for (uint64_t i = (uint64_t)blockIdx.x * kCons + threadIdx.x; i < nres; i += (uint64_t)gridDim.x * kCons) {
-            const uint64_t rr = i / (C / 8), piece = i % (C / 8);
-            const uint64_t o = rr / (uint64_t)q.R, t = rr % (uint64_t)q.R;
-            *reinterpret_cast<uint4*>(out + ((o * T32 + Tq32 + t) * C + piece * 8)) = rs[i];
-        }
-        return;
-    }
-
-    // ---- block partial over the consumer warps, then the fused final reduction
-    __shared__ double w1[NCW], w2[NCW], wm[NCW];
-    __shared__ bool s_last;
-    double d1, d2, dm;
-    warp_partial(A, d1, d2, dm);
-    if (lane == 0) { w1[warp] = d1; w2[warp] = d2; wm[warp] = dm; }
-    asm volatile("bar.sync 1, %0;" ::"r"(kCons) : "memory");
-    if (threadIdx.x == 0) {
-        Partial pp = {0.0, 0.0, 0.0};
-        for (int i = 0; i < NCW; ++i) { pp.s1 += w1[i]; pp.s2 += w2[i]; pp.mx = fmax(pp.mx, wm[i]); }
-        partials[blockIdx.x] = pp;
-        __threadfence();
-        s_last = atomicAdd(done, 1u) == gridDim.x - 1;
-    }
-    asm volatile("bar.sync 1, %0;" ::"r"(kCons) : "memory");
-    if (!s_last || warp != 0) return;
-    __threadfence();
-    // warp 0 of the last CTA: partials in a fixed order (lane l takes l, l+32, ...), then a fixed tree
-    double f1 = 0.0, f2 = 0.0, fm = 0.0;
-    for (uint32_t i = lane; i < gridDim.x; i += 32) {
-        f1 += __ldcg(&partials[i].s1);
-        f2 += __ldcg(&partials[i].s2);
-        fm = fmax(fm, __ldcg(&partials[i].mx));
-    }
-    for (int o2 = 16; o2 > 0; o2 >>= 1) {
-        f1 += __shfl_xor_sync(0xFFFFFFFFu, f1, o2);
-        f2 += __shfl_xor_sync(0xFFFFFFFFu, f2, o2);
-        fm = fmax(fm, __shfl_xor_sync(0xFFFFFFFFu, fm, o2));
-    }
-    if (lane == 0) {
-        const double N = (double)q.outer * (double)q.T * (double)q.C;
-        out_dev->rmse = sqrt(f2 / N);
-        out_dev->max_abs = fm;
-        out_dev->mean_abs = f1 / N;
+    const uint64_t nres = (uint64_t)q.outer * (uint64_t)q.R * (C / 8);
+    const uint4* rs = static_cast<const uint4*>(a.resid);
+    for (uint64_t i = (uint64_t)blockIdx.x * kCons + threadIdx.x; i < nres; i += (uint64_t)gridDim.x * kCons) {
+        const uint64_t rr = i / (C / 8), piece = i % (C / 8);
+        const uint64_t o = rr / (uint64_t)q.R, t = rr % (uint64_t)q.R;
+        *reinterpret_cast<uint4*>(out + ((o * T32 + Tq32 + t) * C + piece * 8)) = rs[i];
     }
 }
 
@@ -1698,30 +1649,29 @@ struct WdsL {
     };
 };
 
-// ---- warp-specialised dequantize / statistics along C
+// ---- warp-specialised dequantize along C
 bool wds_c_ok(const QSpec& q) {
     return q.axis == KVQ_GROUP_ALONG_C && q.x_dt == KVQ_BF16 && q.aligned && q.C == 128 &&
            (q.g == 32 || q.g == 64 || q.g == 128) && meta_kind(q) >= 0 && q.Tq > 0 &&
            q.outer * ((q.Tq + kDcRows - 1) / kDcRows) < (int64_t(1) << 31) && q.outer * q.T < (int64_t(1) << 31);
 }
 
-template <bool STATS>
 struct WdcL {
     template <int B, bool A, int S, int Z> struct L {
         template <int G>
-        static void go(const QArgs& a, const DsStats& ctx, cudaStream_t st) {
-            using Sh = DcShape<B, STATS>;
-            auto kernel = wds_c_kernel<B, A, G, STATS, S, Z>;
+        static void go(const QArgs& a, cudaStream_t st) {
+            using Sh = DcShape<B>;
+            auto kernel = wds_c_kernel<B, A, G, S, Z>;
             if (!ensure_smem(kernel, Sh::kSmem)) return;        // the error stays the last error
             const uint64_t nchunks = (uint64_t)a.q.outer * ((a.q.Tq + kDcRows - 1) / kDcRows);
             const unsigned grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(nchunks, (uint64_t)sm_count()));
-            kernel<<<grid, Sh::kThreads, Sh::kSmem, st>>>(a, ctx.partials, ctx.done, ctx.out);
+            kernel<<<grid, Sh::kThreads, Sh::kSmem, st>>>(a);
         }
-        static void run(const QArgs& a, const DsStats& ctx, cudaStream_t st) {
+        static void run(const QArgs& a, const DsStats&, cudaStream_t st) {
             switch (a.q.g) {
-            case 32: go<32>(a, ctx, st); break;
-            case 64: go<64>(a, ctx, st); break;
-            default: go<128>(a, ctx, st); break;
+            case 32: go<32>(a, st); break;
+            case 64: go<64>(a, st); break;
+            default: go<128>(a, st); break;
             }
         }
     };
@@ -1749,7 +1699,7 @@ bool stream_dequant_supported(const QSpec& q, int out_dt) { return out_dt == KVQ
 cudaError_t stream_dequantize(const QArgs& a, cudaStream_t st)
 {
     if (wds_t_ok(a.q)) by_meta_ctx<WdsL<false>::L>(a, DsStats{nullptr, nullptr, nullptr}, st);
-    else if (wds_c_ok(a.q)) by_meta_ctx<WdcL<false>::L>(a, DsStats{nullptr, nullptr, nullptr}, st);
+    else if (wds_c_ok(a.q)) by_meta_ctx<WdcL::L>(a, DsStats{nullptr, nullptr, nullptr}, st);
     else by_meta_ctx<DsL<false>::L>(a, DsStats{nullptr, nullptr, nullptr}, st);
     return cudaGetLastError();
 }
