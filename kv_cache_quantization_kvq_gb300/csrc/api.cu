@@ -238,7 +238,7 @@ extern "C" {
 
 const char* kvq_last_error(void) { return g_last_error.c_str(); }
 
-const char* kvq_version(void) { return "kvq 0.1.0 (sm_103a)"; }
+const char* kvq_version(void) { return "kvq 0.2.0 (sm_103a)"; }
 
 kvq_status kvq_wait_timeouts(uint64_t* count)
 {
