@@ -306,6 +306,13 @@ def run_ours(args, rank, world, local_rank):
         return {"metric": METRIC, "unit": UNIT, "n_gpus": 1, "data": "synthetic",
                 "config": {"workload": "kivi_int4 decode attention [b8,h8,T8192,d128,g64,R128]", "only": "attend"},
                 "configs": run_configs(b, dev, stream, flush, only_attend=True)}
+    if args.only == "mixed":
+        # the mixed-precision rows alone (profiling)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+        return {"metric": METRIC, "unit": UNIT, "n_gpus": 1, "data": "synthetic",
+                "config": {"workload": "kivi_int4 keys, per-token mixed precision [b8,h8,T8192,d128]", "only": "mixed"},
+                "configs": run_configs(b, dev, stream, flush, only_mixed=True)}
     if args.only == "rotate":
         # the rotation rows alone (profiling)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -536,14 +543,15 @@ def quant_bytes(shape, x_es, cB, sB, zB, rB):
 
 
 def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32, only_attend=False,
-                only_rotate=False):
+                only_rotate=False, only_mixed=False):
     """Median over `runs` (L2 flushed before each) of every op of the large
     configurations: KIVI INT4 (2), full-model INT8 per channel (3), the
     group / bit-width sweep (4), H2O / SnapKV (5); the tiny one (1) in us.
     only_fullmodel: the full-model rows alone, with `layers` layers;
     only_attend: the fused decode attention over the KIVI cache alone;
     only_rotate: the rotation rows (stand-alone, and fused into the value
-    cache's quantize / dequantize) alone."""
+    cache's quantize / dequantize) alone; only_mixed: the per-token mixed
+    precision rows alone."""
     import torch
     from kv_cache_quantization_kvq_gb300 import workloads as W
     peak, _ = measured_peak()
@@ -611,8 +619,31 @@ def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32,
                                                        fq_B)
         del rot, qvf, vout
 
+    def mixed_rows():
+        # per-token mixed precision of the key cache, the four levels in equal shares
+        # (seeded tags): quantize reads K and writes the records, dequantize the reverse
+        shp = tuple(K.shape)
+        tags = torch.randint(0, 4, shp[:2], dtype=torch.uint8, device=dev, generator=torch.Generator(device=dev).manual_seed(4))
+        sB, oB, tB = b.kvq_mixed_sizes(shp)
+        mbuf = torch.empty(sB, dtype=torch.uint8, device=dev)
+        moff = torch.empty(oB // 8, dtype=torch.int64, device=dev)
+        mt2 = torch.empty(tB, dtype=torch.uint8, device=dev)
+        mout = torch.empty_like(K)
+        b.kvq_mixed_quantize(K, tags, shp, mbuf, moff, mt2, stream)
+        torch.cuda.synchronize()
+        used = int(moff.view(shp[0], shp[1] + 1)[:, -1].sum().item())      # record bytes of all slices
+        mq_B = K.numel() * 2 + tags.numel() + used + oB + tB
+        out["2_kivi_int4/K/mixed_quantize"] = entry(med(lambda: b.kvq_mixed_quantize(K, tags, shp, mbuf, moff, mt2, stream)), mq_B)
+        out["2_kivi_int4/K/mixed_dequantize"] = entry(med(lambda: b.kvq_mixed_dequantize(mbuf, moff, mt2, shp, mout, stream)),
+                                                      used + oB + tB + K.numel() * 2)
+        out["2_kivi_int4/K/mixed_bytes_per_number"] = round((used + tB) / K.numel(), 6)
+        del mbuf, moff, mt2, mout, tags
+
     if only_rotate:
         rotate_rows()
+        return out
+    if only_mixed:
+        mixed_rows()
         return out
     if not only_attend:
         for axis, x, name in ((b.ALONG_T, K, "K"), (b.ALONG_C, V, "V")):
@@ -661,24 +692,7 @@ def run_configs(b, dev, stream, flush, runs=20, only_fullmodel=False, layers=32,
     ms = med(decode_steps)
     out["2_kivi_int4/append_KV_one_token_us"] = round(1e3 * ms / 64, 2)
     del stores, aws, app, ksteps, vsteps
-    # per-token mixed precision of the key cache, the four levels in equal shares
-    # (seeded tags): quantize reads K and writes the records, dequantize the reverse
-    shp = tuple(K.shape)
-    tags = torch.randint(0, 4, shp[:2], dtype=torch.uint8, device=dev, generator=torch.Generator(device=dev).manual_seed(4))
-    sB, oB, tB = b.kvq_mixed_sizes(shp)
-    mbuf = torch.empty(sB, dtype=torch.uint8, device=dev)
-    moff = torch.empty(oB // 8, dtype=torch.int64, device=dev)
-    mt2 = torch.empty(tB, dtype=torch.uint8, device=dev)
-    mout = torch.empty_like(K)
-    b.kvq_mixed_quantize(K, tags, shp, mbuf, moff, mt2, stream)
-    torch.cuda.synchronize()
-    used = int(moff.view(shp[0], shp[1] + 1)[:, -1].sum().item())      # record bytes of all slices
-    mq_B = K.numel() * 2 + tags.numel() + used + oB + tB
-    out["2_kivi_int4/K/mixed_quantize"] = entry(med(lambda: b.kvq_mixed_quantize(K, tags, shp, mbuf, moff, mt2, stream)), mq_B)
-    out["2_kivi_int4/K/mixed_dequantize"] = entry(med(lambda: b.kvq_mixed_dequantize(mbuf, moff, mt2, shp, mout, stream)),
-                                                  used + oB + tB + K.numel() * 2)
-    out["2_kivi_int4/K/mixed_bytes_per_number"] = round((used + tB) / K.numel(), 6)
-    del mbuf, moff, mt2, mout, tags
+    mixed_rows()
     rotate_rows()
     del K, V
     # 3: full model INT8, per channel over all tokens
@@ -1001,10 +1015,11 @@ def main():
                          "branches of the step graph")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue the timed steps as plain C-ABI calls instead of replaying a captured CUDA graph")
-    ap.add_argument("--only", choices=("all", "kivi", "evict", "fullmodel", "attend", "rotate"), default="all",
+    ap.add_argument("--only", choices=("all", "kivi", "evict", "fullmodel", "attend", "rotate", "mixed"), default="all",
                     help="time only the KIVI phases or only the eviction phases (profiling); "
-                         "fullmodel / attend / rotate: only the full-model INT8 rows / the fused decode-attention "
-                         "rows / the rotation rows of the per-configuration table")
+                         "fullmodel / attend / rotate / mixed: only the full-model INT8 rows / the fused "
+                         "decode-attention rows / the rotation rows / the mixed-precision rows of the "
+                         "per-configuration table")
     ap.add_argument("--fullmodel-layers", type=int, default=32,
                     help="layers of the full-model INT8 workload with --only fullmodel (a smaller profiling case)")
     ap.add_argument("--evict-tokens", type=int, default=None,
