@@ -353,6 +353,36 @@ def test_append_kv_rejected_before_launch(kb):
         assert (t.value, r.value) == (a["tq"], a["nres"]), kw
 
 
+def test_kv_appender_reports_errors_and_keeps_counters(kb):
+    """KVAppender: a rejected call raises KvqError and leaves tq / nres as they were."""
+    fake = 1 << 20
+
+    class FakeTensor:                           # only data_ptr() and numel() are used
+        def __init__(self, p, n=0):
+            self.p, self.n = p, n
+
+        def data_ptr(self):
+            return self.p
+
+        def numel(self):
+            return self.n
+
+    shape = (2, 256, 128)
+    kq = kb.QParams.asym(4, 0, 15, axis=kb.ALONG_T, group=64, residual=128, scale_dtype=kb.BF16, zero_dtype=kb.BF16)
+    vq = kb.QParams.asym(4, 0, 15, axis=kb.ALONG_C, group=64, residual=128, scale_dtype=kb.BF16, zero_dtype=kb.BF16)
+    bufs = tuple(FakeTensor(fake) for _ in range(4))
+    ws = FakeTensor(fake, kb.kvq_append_kv_workspace(shape, kb.BF16, kq, vq, 64))
+    app = kb.KVAppender(shape, kb.BF16, kq, vq, 64, bufs, bufs, ws, tq=0, nres=191, stream=0)
+    with pytest.raises(kb.KvqError) as e:
+        app.append(FakeTensor(fake + 1), FakeTensor(fake), 1)      # misaligned rows: rejected before launch
+    assert e.value.status == kb.EINVAL
+    assert (app.tq, app.nres) == (0, 191)
+    app.set_counters(3, 0)
+    with pytest.raises(kb.KvqError) as e:
+        app.append(FakeTensor(fake), FakeTensor(fake), 1)          # tq not a multiple of block
+    assert e.value.status == kb.EINVAL and (app.tq, app.nres) == (3, 0)
+
+
 def test_mixed_rejected_before_launch(kb):
     fake = 1 << 20
     assert kb.kvq_mixed_sizes((2, 10, 128)) == (2 * 10 * 128 * 2, 2 * 11 * 8, 2 * 3)
