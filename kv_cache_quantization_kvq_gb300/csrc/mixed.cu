@@ -216,8 +216,16 @@ mixed_quant_kernel(const __nv_bfloat16* x, const uint8_t* tags, int64_t T, int64
     const int64_t t_lo = (int64_t)blockIdx.x * chunk, t_hi = min(T, t_lo + chunk);
     const uint8_t* tg = tags + o * T;
     uint8_t* sl = stream + o * T * 2 * C;
+    // the source rows of a sub-round are contiguous: the first one into L2 now,
+    // each following one a sub-round ahead, so the bucketed loads hit L2
+    auto prefetch_rows = [&](int64_t r0) {
+        if (tid == 0 && r0 < t_hi)
+            bulk_prefetch_l2(x + ((uint64_t)o * T + r0) * C, (uint32_t)min((int64_t)SUB, t_hi - r0) * (uint32_t)(2 * C));
+    };
+    prefetch_rows(t_lo);
     int64_t base = bytes_before(tg, t_lo, C, red);
     for (int64_t sr = t_lo; sr < t_hi; sr += SUB) {
+        prefetch_rows(sr + SUB);
         const int n = (int)min((int64_t)SUB, t_hi - sr);
         const int g = tid < n ? (tg[sr + tid] & 3) : -1;
         if (tid < 4) cnt[tid] = 0;
